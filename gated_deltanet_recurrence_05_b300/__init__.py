@@ -1,0 +1,180 @@
+"""B300-native Gated DeltaNet forward recurrence: Python binding of libgdn.so.
+
+The operation (see include/gdn.h for the full contract): per sequence and value
+head, with the fp32 state S of shape d_k x d_v,
+
+    S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+    o_t = scale S_t^T q_t
+
+This module only marshals arguments: it allocates outputs with torch (device
+memory and streams are torch's job here) and passes raw device pointers to the
+C ABI. Every step of the computation runs in the library's CUDA kernels; there
+is no CPU or PyTorch fallback, and a missing or unloadable library raises.
+
+Entry points (same names as the C ABI, without the ``gdn_`` prefix):
+  chunk_fwd(q, k, v, g, beta, ...)          prefill -> (o, final_state)
+  decode_step(q, k, v, g, beta, state, ...) one token, state updated in place
+  plan_seq_order(cu_seqlens)                longest-first schedule (host)
+  get_device_error(stream=None)             device-side error bits
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = ["chunk_fwd", "decode_step", "plan_seq_order", "get_device_error", "lib",
+           "GdnError", "LIB_PATH", "F32", "BF16", "FLAG_FORCE_SIMT"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
+F32, BF16 = 0, 1
+FLAG_FORCE_SIMT = 1
+_STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
+           4: "GDN_ERR_TIMEOUT"}
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {_STATUS.get(status, status)}")
+        self.status = status
+
+
+def lib():
+    """Load libgdn.so (built in-tree by ``build.py``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libgdn.so not found at {LIB_PATH}; run "
+                              "`python gated_deltanet_recurrence_05_b300/build.py`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        L.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32,
+                                    I32, I32, F, I32, I32, P]
+        L.gdn_chunk_fwd.restype = ctypes.c_int
+        L.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, F, P]
+        L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_plan_seq_order.argtypes = [P, I32, P]
+        L.gdn_plan_seq_order.restype = ctypes.c_int
+        L.gdn_get_device_error.argtypes = [P, P]
+        L.gdn_get_device_error.restype = ctypes.c_int
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_version.restype = I32
+        _lib = L
+    return _lib
+
+
+def _code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise GdnError(fn, status)
+
+
+def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+              beta: torch.Tensor, initial_state: Optional[torch.Tensor] = None,
+              cu_seqlens: Optional[torch.Tensor] = None, *, num_seqs: Optional[int] = None,
+              seq_order: Optional[torch.Tensor] = None, output_dtype: Optional[torch.dtype] = None,
+              scale: float = 0.0, chunk_size: int = 0, output_final_state: bool = True,
+              out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None,
+              force_simt: bool = False, stream=None):
+    """Prefill of the recurrence over packed tokens (see include/gdn.h).
+
+    q, k: [T, H_qk, d_k]; v: [T, H_v, d_v] (fp32 or bf16, one dtype); g, beta:
+    [T, H_v] fp32; initial_state: [N, H_v, d_k, d_v] fp32 or None; cu_seqlens:
+    [N+1] int32 CUDA tensor or None (then ``num_seqs`` equal-length sequences,
+    default 1). Returns (o [T, H_v, d_v], final_state or None).
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _dev(t, name)
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    if cu_seqlens is not None:
+        _dev(cu_seqlens, "cu_seqlens")
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    if seq_order is not None:
+        _dev(seq_order, "seq_order")
+    if initial_state is not None:
+        _dev(initial_state, "initial_state")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    odt = output_dtype or v.dtype
+    o = out if out is not None else torch.empty((T, h_v, d_v), dtype=odt, device=v.device)
+    fs = None
+    if output_final_state:
+        fs = final_state_out if final_state_out is not None else torch.empty(
+            (N, h_v, d_k, d_v), dtype=torch.float32, device=v.device)
+    st = lib().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                             _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(fs), N, T, h_qk, h_v,
+                             d_k, d_v, _code(q), _code(o), float(scale), int(chunk_size),
+                             FLAG_FORCE_SIMT if force_simt else 0, _stream(stream))
+    _check("gdn_chunk_fwd", st)
+    return o, fs
+
+
+def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                beta: torch.Tensor, state: torch.Tensor, *, output_dtype: Optional[torch.dtype] = None,
+                scale: float = 0.0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One token for N sequences; ``state`` [N, H_v, d_k, d_v] is updated in place.
+
+    q, k: [N, H_qk, d_k]; v: [N, H_v, d_v]; g, beta: [N, H_v] fp32. Returns o [N, H_v, d_v].
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
+        _dev(t, name)
+    N, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    odt = output_dtype or v.dtype
+    o = out if out is not None else torch.empty((N, h_v, d_v), dtype=odt, device=v.device)
+    st = lib().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o),
+                               N, h_qk, h_v, d_k, d_v, _code(q), _code(o), float(scale),
+                               _stream(stream))
+    _check("gdn_decode_step", st)
+    return o
+
+
+def plan_seq_order(cu_seqlens) -> torch.Tensor:
+    """Longest-first schedule of the sequences (host computation in the library).
+
+    Accepts a CPU tensor / list of N+1 offsets; returns an int32 CPU tensor [N]."""
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).cpu().contiguous()
+    N = cu.numel() - 1
+    order = torch.empty(max(N, 0), dtype=torch.int32)
+    _check("gdn_plan_seq_order", lib().gdn_plan_seq_order(_ptr(cu), N, _ptr(order)))
+    return order
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the GDN_DEVERR_* bits."""
+    code = ctypes.c_uint32(0)
+    _check("gdn_get_device_error", lib().gdn_get_device_error(_stream(stream), ctypes.byref(code)))
+    return int(code.value)

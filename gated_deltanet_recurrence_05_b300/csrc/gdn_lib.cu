@@ -1,0 +1,180 @@
+// C ABI of the GDN library: argument checks on the host, kernel dispatch.
+// Declarations and the contract of every entry point: include/gdn.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <numeric>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+#include "gdn_decode.cuh"
+#include "gdn_chunk_simt.cuh"
+#include "gdn_chunk_tc.cuh"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+bool ok_dtype(int32_t d) { return d == GDN_F32 || d == GDN_BF16; }
+
+// Query (once per device) the opt-in shared-memory limit and SM count.
+struct DevInfo { int smem_optin = 0; int sms = 0; };
+DevInfo dev_info() {
+    int dev = 0;
+    DevInfo di;
+    if (cudaGetDevice(&dev) != cudaSuccess) return di;
+    cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    return di;
+}
+
+template <typename TIn, typename TOut>
+gdn_status launch_simt(const gdn::SimtArgs& a, size_t smem, cudaStream_t s) {
+    auto kern = gdn::chunk_simt_kernel<TIn, TOut>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const long long blocks = (long long)a.num_seqs * a.h_v * a.n_tiles;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    kern<<<(unsigned)blocks, 256, smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename TIn, typename TOut>
+gdn_status launch_decode(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, float* state, void* o, int N, int h_qk, int h_v,
+                         int d_k, int d_v, float scale, cudaStream_t s) {
+    const long long blocks = (long long)N * h_v;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const int grp = h_v / h_qk;
+    if (d_k == 128 && d_v == 128) {
+        gdn::decode_d128_kernel<TIn, TOut><<<(unsigned)blocks, 256, 0, s>>>(
+            static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
+            state, static_cast<TOut*>(o), h_qk, h_v, grp, scale);
+    } else {
+        gdn::decode_generic_kernel<TIn, TOut><<<(unsigned)blocks, 128, 0, s>>>(
+            static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
+            state, static_cast<TOut*>(o), h_qk, h_v, grp, d_k, d_v, scale);
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+        case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+        case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+        case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    }
+    return "GDN_ERR_UNKNOWN";
+}
+
+int32_t gdn_version(void) { return 100; }
+
+gdn_status gdn_plan_seq_order(const int32_t* cu, int32_t num_seqs, int32_t* order_out) {
+    if (num_seqs < 0 || (num_seqs > 0 && (cu == nullptr || order_out == nullptr))) return GDN_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < num_seqs; ++n)
+        if (cu[n + 1] < cu[n]) return GDN_ERR_INVALID_ARG;
+    std::vector<int32_t> idx(num_seqs);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+        return (cu[a + 1] - cu[a]) > (cu[b + 1] - cu[b]);
+    });
+    std::copy(idx.begin(), idx.end(), order_out);
+    return GDN_OK;
+}
+
+gdn_status gdn_get_device_error(void* stream, uint32_t* code) {
+    if (code == nullptr) return GDN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, gdn::g_device_error, sizeof v) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaMemcpyToSymbol(gdn::g_device_error, &zero, sizeof zero) != cudaSuccess) return GDN_ERR_CUDA;
+    *code = v;
+    return GDN_OK;
+}
+
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, void* o, int32_t num_seqs,
+                           int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                           int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream) {
+    if (num_seqs < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
+    if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return GDN_OK;
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g) || !ok_ptr(beta) || !ok_ptr(state) || !ok_ptr(o))
+        return GDN_ERR_INVALID_ARG;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bf_in = dtype_qkv == GDN_BF16, bf_out = dtype_o == GDN_BF16;
+    if (bf_in && bf_out)
+        return launch_decode<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+    if (bf_in)
+        return launch_decode<__nv_bfloat16, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+    if (bf_out)
+        return launch_decode<float, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+    return launch_decode<float, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+}
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                         const int32_t* seq_order, void* o, float* final_state, int32_t num_seqs,
+                         int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                         int32_t dtype_qkv, int32_t dtype_o, float scale, int32_t chunk_size,
+                         int32_t flags, void* stream) {
+    if (num_seqs < 0 || total_tokens < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
+    if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDN_ERR_INVALID_ARG;
+    if (flags & ~GDN_FLAG_FORCE_SIMT) return GDN_ERR_INVALID_ARG;
+    if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g) || !ok_ptr(beta) || !ok_ptr(o)))
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_opt(initial_state) || !ok_opt(final_state) || !ok_opt(cu_seqlens) || !ok_opt(seq_order))
+        return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
+    if (total_tokens == 0 && final_state == nullptr) return GDN_OK;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
+    const int C = chunk_size == 0 ? 64 : chunk_size;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long eq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
+
+    const bool bf_in = dtype_qkv == GDN_BF16, bf_out = dtype_o == GDN_BF16;
+    if (bf_in && d_k == 128 && d_v == 128 && !(flags & GDN_FLAG_FORCE_SIMT) && gdn::tc_available()) {
+        gdn::TcArgs a{};
+        a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = initial_state;
+        a.cu = cu_seqlens; a.order = seq_order; a.o = o; a.hT = final_state;
+        a.num_seqs = num_seqs; a.total = total_tokens; a.eq_len = eq_len;
+        a.h_qk = h_qk; a.h_v = h_v; a.grp = h_v / h_qk; a.scale = scale;
+        return gdn::launch_tc(a, bf_out, s);
+    }
+
+    gdn::SimtArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = initial_state;
+    a.cu = cu_seqlens; a.order = seq_order; a.o = o; a.hT = final_state;
+    a.num_seqs = num_seqs; a.total = total_tokens; a.eq_len = eq_len;
+    a.h_qk = h_qk; a.h_v = h_v; a.d_k = d_k; a.d_v = d_v; a.grp = h_v / h_qk;
+    a.C = C; a.dvt = d_v < 64 ? d_v : 64; a.n_tiles = (d_v + a.dvt - 1) / a.dvt; a.scale = scale;
+    const size_t smem = gdn::simt_smem_floats(C, d_k, a.dvt) * sizeof(float);
+    const DevInfo di = dev_info();
+    if (di.smem_optin <= 0) return GDN_ERR_CUDA;
+    if (smem > (size_t)di.smem_optin) return GDN_ERR_UNSUPPORTED;
+    if (bf_in && bf_out) return launch_simt<__nv_bfloat16, __nv_bfloat16>(a, smem, s);
+    if (bf_in) return launch_simt<__nv_bfloat16, float>(a, smem, s);
+    if (bf_out) return launch_simt<float, __nv_bfloat16>(a, smem, s);
+    return launch_simt<float, float>(a, smem, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,155 @@
+/*
+ * gdn.h -- C ABI of the B300 (sm_103a) Gated DeltaNet forward recurrence.
+ *
+ * The operation (per sequence n and value head h, with the state S of shape
+ * d_k x d_v, rows indexed by the key dimension):
+ *
+ *     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t,        alpha_t = exp(g_t)
+ *
+ * This is the gated delta rule described in the podcast episode
+ * "Qwen3.8-Next design: hybrid attention, residuals and n-gram embeddings",
+ * transcript segment 14 (a decay alpha erases part of the whole state each
+ * step; the delta term reads what is stored under the current key, subtracts
+ * it and writes only the error), used as the recurrent token mixer in three of
+ * every four layers (same episode, segment 4; "On the Design of Qwen3.8-Next
+ * Architecture", abstract). The pages give it in words only; the d_k x d_v
+ * orientation above is the one under which a value written under a unit key
+ * is read back by S^T k.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers, dense row-major, 16-byte aligned.
+ *    The caller owns every buffer; the library never allocates device memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
+ *    the legacy default stream). Argument checks run on the host before any
+ *    launch; on any error status nothing has been launched.
+ *  - q/k are used as given (L2-normalisation, if wanted, is the caller's).
+ *    g is the log-decay (alpha = exp(g)); g <= 0 is expected, not enforced.
+ *  - Value head h reads q/k head h / (H_v / H_qk) (contiguous groups, the
+ *    GQA-style sharing of one q/k head by H_v/H_qk value heads).
+ *  - dtype codes: GDN_F32 = fp32, GDN_BF16 = bf16. g, beta and all states are
+ *    always fp32.
+ *  - Faults found on the device (a cu_seqlens entry out of range, an internal
+ *    wait that ran out) do not stop the stream: the kernel skips the affected
+ *    work and records a code that gdn_get_device_error() returns.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad code   */
+    GDN_ERR_UNSUPPORTED = 2,   /* valid but not compiled (e.g. d_k > 128)       */
+    GDN_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed          */
+    GDN_ERR_TIMEOUT = 4        /* reported by gdn_get_device_error only         */
+} gdn_status;
+
+enum { GDN_F32 = 0, GDN_BF16 = 1 };
+
+/* Flags for gdn_chunk_fwd. */
+enum {
+    GDN_FLAG_FORCE_SIMT = 1    /* use the fp32 CUDA-core chunk kernel even where
+                                  the tensor-core kernel applies (cross-checks) */
+};
+
+/* Device error codes (bit set) returned by gdn_get_device_error. */
+enum {
+    GDN_DEVERR_SEQLENS = 1,    /* cu_seqlens / seq_order entry out of range     */
+    GDN_DEVERR_TIMEOUT = 2     /* an mbarrier wait exceeded its iteration limit */
+};
+
+/*
+ * gdn_chunk_fwd -- chunkwise-parallel prefill of the recurrence.
+ *
+ * q, k          [T_total, H_qk, d_k]  dtype_qkv
+ * v             [T_total, H_v, d_v]   dtype_qkv
+ * g, beta       [T_total, H_v]        fp32 (log-decay, write strength)
+ * initial_state [N, H_v, d_k, d_v]    fp32, NULL = zero state
+ * cu_seqlens    [N + 1]               int32 device array of sequence starts
+ *               (cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T_total);
+ *               NULL = N sequences of equal length T_total / N
+ * seq_order     [N]                   int32 device permutation of 0..N-1: the
+ *               order in which sequences are scheduled (longest first keeps
+ *               the tail short; see gdn_plan_seq_order). NULL = 0..N-1.
+ * o             [T_total, H_v, d_v]   dtype_o (written)
+ * final_state   [N, H_v, d_k, d_v]    fp32 (written), NULL = not written.
+ *               final_state == initial_state (in place) is allowed.
+ * scale         output scale; 0 selects 1/sqrt(d_k)
+ * chunk_size    0 (= 64), 16, 32 or 64. The result does not depend on it beyond
+ *               rounding. The tensor-core kernel (bf16 q/k/v, d_k = d_v = 128)
+ *               always uses 64; the CUDA-core kernel uses the value given.
+ *
+ * Kernels: bf16 inputs with d_k = d_v = 128 run the tcgen05/TMEM kernel with
+ * TMA-fed tiles and the fp32 state kept on chip across chunks; everything else
+ * (fp32 inputs, other head sizes up to 128) runs the fp32 CUDA-core kernel.
+ * Returns GDN_ERR_INVALID_ARG for null/misaligned pointers, H_v % H_qk != 0,
+ * N < 0, T_total < 0, T_total % N != 0 without cu_seqlens, or bad codes;
+ * GDN_ERR_UNSUPPORTED for d_k or d_v outside 1..128.
+ */
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v,
+                         const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         const int32_t* seq_order,
+                         void* o, float* final_state,
+                         int32_t num_seqs, int64_t total_tokens,
+                         int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                         int32_t dtype_qkv, int32_t dtype_o,
+                         float scale, int32_t chunk_size, int32_t flags,
+                         void* stream);
+
+/*
+ * gdn_decode_step -- one token of the recurrence for N independent sequences,
+ * updating the states in place (one read and one write of each state).
+ *
+ * q, k    [N, H_qk, d_k] dtype_qkv     v [N, H_v, d_v] dtype_qkv
+ * g, beta [N, H_v] fp32
+ * state   [N, H_v, d_k, d_v] fp32, read and overwritten with the new state
+ * o       [N, H_v, d_v] dtype_o (written)
+ * scale   0 selects 1/sqrt(d_k)
+ *
+ * d_k = d_v = 128 runs the bandwidth-bound kernel (128-bit coalesced state
+ * traffic, warp-shuffle reductions); other sizes up to 128 run a simpler
+ * kernel. Errors as for gdn_chunk_fwd.
+ */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v,
+                           const float* g, const float* beta,
+                           float* state, void* o,
+                           int32_t num_seqs, int32_t h_qk, int32_t h_v,
+                           int32_t d_k, int32_t d_v,
+                           int32_t dtype_qkv, int32_t dtype_o, float scale,
+                           void* stream);
+
+/*
+ * gdn_plan_seq_order -- HOST helper: writes into order_out[0..N-1] (host
+ * memory) the sequence indices sorted by length, longest first (ties keep
+ * index order), from a HOST copy of cu_seqlens [N + 1]. The caller copies the
+ * result to the device and passes it as seq_order.
+ */
+gdn_status gdn_plan_seq_order(const int32_t* cu_seqlens_host, int32_t num_seqs,
+                              int32_t* order_out);
+
+/*
+ * gdn_get_device_error -- synchronises `stream`, then returns in *code the
+ * GDN_DEVERR_* bits recorded by kernels of this library on the current
+ * device since the last call, and clears them.
+ */
+gdn_status gdn_get_device_error(void* stream, uint32_t* code);
+
+/* Human-readable name of a status code (static string). */
+const char* gdn_status_string(gdn_status s);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load, export every entry point that include/gdn.h declares,
+and reject bad arguments on the host with the documented status before it
+touches the device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_deltanet_recurrence_05_b300 as gdn
+from gated_deltanet_recurrence_05_b300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_plan_seq_order",
+                 "gdn_get_device_error", "gdn_status_string", "gdn_version"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings_and_version(L):
+    assert L.gdn_status_string(0) == b"GDN_OK"
+    assert L.gdn_status_string(2) == b"GDN_ERR_UNSUPPORTED"
+    assert L.gdn_version() >= 100
+
+
+def test_plan_seq_order_longest_first(L):
+    cu = [0, 5, 5, 17, 20, 32]  # lengths 5, 0, 12, 3, 12
+    order = gdn.plan_seq_order(cu).tolist()
+    assert order == [2, 4, 0, 3, 1]
+
+
+def test_plan_seq_order_rejects_decreasing(L):
+    with pytest.raises(gdn.GdnError):
+        gdn.plan_seq_order([0, 4, 3])
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
+
+
+def _fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, order=None, o=FAKE,
+             hT=None, N=1, T=64, h_qk=2, h_v=4, d_k=64, d_v=64, dq=1, do=1, scale=0.0,
+             chunk=0, flags=0)
+    a.update(kw)
+    return L.gdn_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["cu"], a["order"],
+                           a["o"], a["hT"], a["N"], a["T"], a["h_qk"], a["h_v"], a["d_k"], a["d_v"],
+                           a["dq"], a["do"], a["scale"], a["chunk"], a["flags"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), INVALID),
+    (dict(v=FAKE + 4), INVALID),                 # misaligned
+    (dict(h0=FAKE + 8), INVALID),
+    (dict(h_qk=3, h_v=4), INVALID),              # H_v % H_qk != 0
+    (dict(h_qk=0), INVALID),
+    (dict(N=-1), INVALID),
+    (dict(T=-5), INVALID),
+    (dict(N=3, T=64), INVALID),                  # equal lengths need T % N == 0
+    (dict(dq=7), INVALID),
+    (dict(do=2), INVALID),
+    (dict(chunk=48), INVALID),
+    (dict(flags=8), INVALID),
+    (dict(d_k=256), UNSUPPORTED),
+    (dict(d_v=129), UNSUPPORTED),
+    (dict(N=0, T=0), OK),                        # nothing to do
+    (dict(N=0, T=5), INVALID),
+    (dict(T=0, hT=None), OK),                    # no tokens, no state requested
+])
+def test_chunk_fwd_host_validation(L, kw, status):
+    assert _fwd(L, **kw) == status
+
+
+def _dec(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, S=FAKE, o=FAKE, N=4, h_qk=2, h_v=4,
+             d_k=128, d_v=128, dq=1, do=1, scale=0.0)
+    a.update(kw)
+    return L.gdn_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S"], a["o"], a["N"],
+                             a["h_qk"], a["h_v"], a["d_k"], a["d_v"], a["dq"], a["do"], a["scale"],
+                             None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(S=None), INVALID),
+    (dict(o=FAKE + 2), INVALID),
+    (dict(h_qk=3), INVALID),
+    (dict(dq=5), INVALID),
+    (dict(d_k=200), UNSUPPORTED),
+    (dict(N=0), OK),
+    (dict(N=-2), INVALID),
+])
+def test_decode_host_validation(L, kw, status):
+    assert _dec(L, **kw) == status
+
+
+def test_binding_rejects_cpu_tensors():
+    x = torch.zeros(4, 1, 8)
+    g = torch.zeros(4, 1)
+    with pytest.raises(ValueError):
+        gdn.chunk_fwd(x, x, x, g, g)
+    with pytest.raises(ValueError):
+        gdn.decode_step(x[:1], x[:1], x[:1], g[:1], g[:1], torch.zeros(1, 1, 8, 8))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(gdn, "_lib", None)
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(ImportError):
+        gdn.lib()
