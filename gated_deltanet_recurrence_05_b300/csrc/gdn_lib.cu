@@ -16,9 +16,12 @@
 
 namespace {
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
-bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+// Non-null and aligned to `a` bytes (16 for tensors read with 128-bit or TMA
+// accesses, the element size for the rest).
+bool ok_ptr(const void* p, uintptr_t a = 16) { return p != nullptr && aligned(p, a); }
+bool ok_opt(const void* p, uintptr_t a = 16) { return p == nullptr || aligned(p, a); }
+uintptr_t esize(int32_t dtype) { return dtype == GDN_BF16 ? 2 : 4; }
 bool ok_dtype(int32_t d) { return d == GDN_F32 || d == GDN_BF16; }
 
 // Query (once per device) the opt-in shared-memory limit and SM count.
@@ -112,7 +115,9 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return GDN_OK;
-    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g) || !ok_ptr(beta) || !ok_ptr(state) || !ok_ptr(o))
+    const uintptr_t ei = esize(dtype_qkv), eo = esize(dtype_o);
+    if (!ok_ptr(q, ei) || !ok_ptr(k, ei) || !ok_ptr(v, ei) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) ||
+        !ok_ptr(state, 16) || !ok_ptr(o, eo))
         return GDN_ERR_INVALID_ARG;
     if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -140,9 +145,10 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
-    if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g) || !ok_ptr(beta) || !ok_ptr(o)))
+    if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g, 4) ||
+                             !ok_ptr(beta, 4) || !ok_ptr(o, esize(dtype_o))))
         return GDN_ERR_INVALID_ARG;
-    if (!ok_opt(initial_state) || !ok_opt(final_state) || !ok_opt(cu_seqlens) || !ok_opt(seq_order))
+    if (!ok_opt(initial_state) || !ok_opt(final_state) || !ok_opt(cu_seqlens, 4) || !ok_opt(seq_order, 4))
         return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
     if (total_tokens == 0 && final_state == nullptr) return GDN_OK;
@@ -152,7 +158,8 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     const long long eq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
 
     const bool bf_in = dtype_qkv == GDN_BF16, bf_out = dtype_o == GDN_BF16;
-    if (bf_in && d_k == 128 && d_v == 128 && !(flags & GDN_FLAG_FORCE_SIMT) && gdn::tc_available()) {
+    if (bf_in && d_k == 128 && d_v == 128 && total_tokens > 0 && !(flags & GDN_FLAG_FORCE_SIMT) &&
+        gdn::tc_available()) {
         gdn::TcArgs a{};
         a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = initial_state;
         a.cu = cu_seqlens; a.order = seq_order; a.o = o; a.hT = final_state;

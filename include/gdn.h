@@ -18,7 +18,10 @@
  * is read back by S^T k.
  *
  * Conventions shared by every call:
- *  - All tensor pointers are DEVICE pointers, dense row-major, 16-byte aligned.
+ *  - All tensor pointers are DEVICE pointers to dense row-major arrays. q, k,
+ *    v of gdn_chunk_fwd and every state pointer must be 16-byte aligned (TMA
+ *    and 128-bit accesses); g, beta, cu_seqlens and seq_order need 4-byte
+ *    alignment, o and the q/k/v of gdn_decode_step their element size.
  *    The caller owns every buffer; the library never allocates device memory.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
  *    the legacy default stream). Argument checks run on the host before any

@@ -29,7 +29,9 @@ def max_err_ratio(got, ref, out_bf16=False) -> float:
     r = rms(ref)
     if out_bf16:
         ref_b = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
-        ulp = np.abs(ref_b) * 2.0 ** -8
+        # one bf16 ulp of |ref_b|: 2^(e - 8) for |x| in [2^(e-1), 2^e) (8 significant bits)
+        _, e = np.frexp(np.abs(ref_b))
+        ulp = np.ldexp(1.0, e - 8)
         excess = np.maximum(np.abs(got - ref_b) - ulp, 0.0)
         return float(excess.max() / r) if got.size else 0.0
     return float(np.abs(got - ref).max() / r) if got.size else 0.0

@@ -76,7 +76,8 @@ def _fwd(L, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(q=None), INVALID),
-    (dict(v=FAKE + 4), INVALID),                 # misaligned
+    (dict(v=FAKE + 4), INVALID),                 # q/k/v need 16 bytes (TMA)
+    (dict(g=FAKE + 2), INVALID),                 # g needs 4 bytes
     (dict(h0=FAKE + 8), INVALID),
     (dict(h_qk=3, h_v=4), INVALID),              # H_v % H_qk != 0
     (dict(h_qk=0), INVALID),
@@ -108,7 +109,8 @@ def _dec(L, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(S=None), INVALID),
-    (dict(o=FAKE + 2), INVALID),
+    (dict(o=FAKE + 1), INVALID),                 # not element-aligned
+    (dict(S=FAKE + 4), INVALID),                 # state needs 16 bytes
     (dict(h_qk=3), INVALID),
     (dict(dq=5), INVALID),
     (dict(d_k=200), UNSUPPORTED),

@@ -47,7 +47,7 @@ def test_decode_full_size_all_pairs():
     configuration of the decode benchmark, 16 consecutive steps, every pair
     checked against the oracle."""
     d = gdn_inputs.make_workload("decode", steps=16)
-    o, S = _run_steps(d, 16)
+    o, S = _run_steps(d, 16, torch.float32)
     o_ref, S_ref = oracle.decode_steps(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"])
     assert_parity(o, o_ref, TAU_BF16, "o")
     assert_parity(S, S_ref, TAU_BF16, "state")
@@ -89,8 +89,9 @@ def test_decode_matches_prefill():
     o_dec, S_dec = _run_steps(d, 40)
     dd = to_cuda(d)
     for n in range(2):
-        o_pf, S_pf = gdn.chunk_fwd(dd["q"][:, n], dd["k"][:, n], dd["v"][:, n], dd["g"][:, n],
-                                   dd["beta"][:, n], dd["state"][n:n + 1])
+        sl = lambda x: x[:, n].contiguous()
+        o_pf, S_pf = gdn.chunk_fwd(sl(dd["q"]), sl(dd["k"]), sl(dd["v"]), sl(dd["g"]),
+                                   sl(dd["beta"]), dd["state"][n:n + 1].contiguous())
         torch.cuda.synchronize()
         assert_parity(o_dec[:, n], o_pf.cpu().numpy(), TAU_F32, "o decode vs prefill")
         assert_parity(S_dec[n], S_pf[0].cpu().numpy(), TAU_F32, "state decode vs prefill")
