@@ -204,7 +204,8 @@ def oracle_sample(w, target_s=12.0, threads=0):
     of a subset of (sequence, value-head) pairs. Returns tokens/s (pair-tokens/s
     divided by H_v), the thread count and a description of the sample."""
     import oracle
-    cores = oracle.max_threads() if threads <= 0 else threads
+    # explicit thread counts on every call: the oracle's OpenMP setting persists
+    cores = len(os.sched_getaffinity(0)) if threads <= 0 else threads
     N, hv = len(w["lengths"]), w["h_v"]
     cu = cu_of(w)
     t = time.perf_counter()
@@ -216,7 +217,7 @@ def oracle_sample(w, target_s=12.0, threads=0):
     pairs = [(i // hv % N, i % hv) for i in range(n_pairs)]
     t = time.perf_counter()
     oracle.recurrent(w["q"], w["k"], w["v"], w["g"], w["beta"], h0=w["h0"], cu_seqlens=cu,
-                     pairs=pairs, threads=threads)
+                     pairs=pairs, threads=cores)
     dt = time.perf_counter() - t
     pair_tokens = sum(w["lengths"][n] for n, _ in pairs)
     return pair_tokens / hv / dt, cores, (
