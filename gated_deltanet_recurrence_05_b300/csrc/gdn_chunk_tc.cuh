@@ -14,36 +14,38 @@
 // Everything is computed in the transposed frame so that every tensor-core
 // product has M = 128 and the state's value dimension lands on TMEM lanes:
 //   X      = [K; Q] K^T                                  (M1, 128x64x128)
-//   W^T    = K^T Bw^T,  Bw = T diag(beta gamma)          (M2, 128x64x64)
+//   -W^T   = K^T Bw^T,  Bw = -T diag(beta gamma)         (M2, 128x64x64)
 //   U^T    = V^T Bu^T,  Bu = T diag(beta)                (M2, 128x64x64)
 //   D^T    = U^T + S^T (-W)^T                            (M3a, 128x64x128)
 //   O^T    = S^T (gamma scale Q)^T + D^T P^T             (M3b + M4)
-//   Sacc   = D^T Kdec,  Kdec = diag(Gamma_last,.) K      (M5, 128x128x64)
+//   Sacc   = (D^T diag(Gamma_last,.)) K                  (M5, 128x128x64)
 //   S^T   <- gamma_last S^T + Sacc                       (fp32, registers)
-// where D^T = Delta^T. Thread j of the state warps owns column j of S (TMEM
-// lane j): its fp32 state lives in registers for the whole sequence; an fp16
-// copy of S^T and of Delta^T is written to TMEM and read there as the A
-// operand of the next products. Only exponentials of G_r - G_s with r >= s are
-// formed, so no factor exceeds 1 for g <= 0.
+// where D^T = Delta^T. Thread (j, half) of the state warps owns half of column
+// j of S (TMEM lane j) in fp32 registers for the whole sequence; fp16 copies
+// of S^T and of Delta^T (plain and decay-scaled) are written to TMEM and read
+// there as the A operand of the next products. Only exponentials of G_r - G_s
+// with r >= s are formed, so no factor exceeds 1 for g <= 0.
+//
+// T = (I + A)^{-1} is solved per 16 x 16 block: diagonal blocks by forward
+// substitution in fp32, off-diagonal blocks on the warp-level tensor-core MMA
+// (fp16 operands, fp32 accumulation), one block-row per warp.
 //
 // Operand precision: every product after X takes fp16 operands (10-bit
 // mantissa) with fp32 accumulation; the bf16 inputs K, Q, V convert to fp16
 // exactly (their magnitudes are far inside the fp16 range), so only the
-// computed operands (S, Delta, T, W, P and the decay-scaled Q and K) are
+// computed operands (S, Delta, T, W, P and the decay-scaled Q and Delta) are
 // rounded, at 2^-11 instead of bf16's 2^-8. Decay-scaled values that fall
 // below the fp16 range contribute less than 1e-7 of the largest terms. The
 // path therefore assumes |v| and |S| stay well below 6e4 (the fp16 range).
 //
-// Warp roles (512 threads):
-//   warp 0      TMA producer: K, Q (3-deep ring) and V (2-deep ring) tiles
-//   warp 1      issues the state-dependent products M3a, M3b, M5, M4; owns TMEM
-//   warp 2      issues the look-ahead products M1 (next chunk) and M2
-//   warp 3      loads g, beta of upcoming chunks; cumulative decay and factors
-//   warps 4-7   prep: A and P from X, T by blocked forward substitution, Bw/Bu,
-//               -W^T, gamma scaling of Q, Kdec
-//   warps 8-15  state: Delta^T and S^T hand-off, fp32 state update, output
-// All waits are bounded (a timeout raises an abort flag, records
-// GDN_DEVERR_TIMEOUT and every role unwinds); TMEM is always freed.
+// Warp roles (640 threads) are listed where they branch (chunk_tc_kernel).
+// Two prep groups work on alternate chunks so that the per-chunk solve, whose
+// steps are short and dependent, overlaps; the state warps convert operands
+// two chunks ahead in the time they would otherwise wait. The instruction
+// footprint is kept small on purpose (rolled issue loops, one copy of each
+// step): with 20 warps running different code the instruction cache was the
+// first bottleneck. All waits are bounded (a timeout raises an abort flag,
+// records GDN_DEVERR_TIMEOUT and every role unwinds); TMEM is always freed.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -65,10 +67,18 @@ struct TcArgs {
 
 namespace tck {
 constexpr int C = 64, D = 128;
-constexpr int KQ_STAGES = 3, V_STAGES = 2, GB_SLOTS = 4;
-constexpr int NTHREADS = 512;
+constexpr int KQ_STAGES = 3, V_STAGES = 2, GB_SLOTS = 3;
+constexpr int NTHREADS = 640;
+// Registers: launched with REGS_LAUNCH per thread (640 x 96 = 61440). The
+// single-thread roles and the prep groups give some up; the two state
+// warpgroups (64 fp32 state values per thread) take them:
+// 128 x (48 + 80 + 80 + 136 + 136) = 61440.
+constexpr int REGS_LAUNCH = 96, REGS_ROLES = 48, REGS_PREP = 80, REGS_STATE = 136;
+static_assert(128 * (REGS_ROLES + 2 * REGS_PREP + 2 * REGS_STATE) <= NTHREADS * REGS_LAUNCH,
+              "register rebalancing exceeds the launch allocation");
 // TMEM columns
-constexpr uint32_t T_SACC = 0, T_DU = 128, T_O = 192, T_X = 256, T_W = 320, T_ST = 384, T_DT = 448;
+constexpr uint32_t T_SACC = 0, T_DU = 128, T_O = 192, T_X = 256, T_W = 320, T_ST = 384, T_DT = 448,
+                   T_DTD = 480;
 constexpr uint32_t TMEM_COLS = 512;
 // shared memory layout (byte offsets from a 1024-aligned base)
 constexpr uint32_t KQ_BYTES = 32768;  // K kb0 | Q kb0 | K kb1 | Q kb1, 8 KB each (64 rows x 128 B)
@@ -76,29 +86,33 @@ constexpr uint32_t V_BYTES = 16384;   // V kb0 | V kb1
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_V = OFF_KQ + KQ_STAGES * KQ_BYTES;
 constexpr uint32_t OFF_WT = OFF_V + V_STAGES * V_BYTES;  // -W^T, MN-major B: 128 rows (i) x 128 B (r)
-constexpr uint32_t OFF_BW = OFF_WT + 16384;              // Bw, K-major B: 64 rows (r) x 128 B (s)
-constexpr uint32_t OFF_BU = OFF_BW + 8192;
-constexpr uint32_t OFF_P = OFF_BU + 8192;                // P x 2 buffers, K-major B
-constexpr uint32_t LDA = 68;                             // fp32 row stride of A and T
-constexpr uint32_t OFF_A = OFF_P + 16384;
-constexpr uint32_t OFF_T = OFF_A + 64 * LDA * 4;
-constexpr uint32_t OFF_GB = OFF_T + 64 * LDA * 4;
+constexpr uint32_t OFF_BW = OFF_WT + 16384;              // Bw x 2 buffers, K-major B: 64 rows (r) x 128 B (s)
+constexpr uint32_t OFF_BU = OFF_BW + 16384;              // Bu x 2 buffers
+constexpr uint32_t OFF_P = OFF_BU + 16384;               // P x 2 buffers, K-major B
+// per prep group (x 2): A fp16 (64 rows x 128 B, 128-byte swizzle), the
+// diagonal 16x16 blocks of A in fp32 (column-major), those of T in fp16
+constexpr uint32_t OFF_AS = OFF_P + 16384;
+constexpr uint32_t OFF_AD = OFF_AS + 2 * 8192;
+constexpr uint32_t OFF_TS = OFF_AD + 2 * 4096;
+constexpr uint32_t OFF_GB = OFF_TS + 2 * 2048;
 constexpr uint32_t GB_FLOATS = 6 * 64 + 4;               // G, gam, bet, bg, dec, qsc, gC
 constexpr uint32_t GB_SLOT_BYTES = GB_FLOATS * 4;
 constexpr uint32_t OFF_BAR = OFF_GB + GB_SLOTS * GB_SLOT_BYTES;
-constexpr uint32_t NUM_BARS = 32;
+constexpr uint32_t NUM_BARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;    // + alignment slack
-static_assert(OFF_WT % 1024 == 0 && OFF_BW % 1024 == 0 && OFF_P % 1024 == 0, "tile alignment");
+static_assert(OFF_WT % 1024 == 0 && OFF_BW % 1024 == 0 && OFF_P % 1024 == 0 && OFF_AS % 1024 == 0,
+              "tile alignment");
+static_assert(GB_SLOT_BYTES % 16 == 0 && OFF_GB % 16 == 0, "gb slot alignment");
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // barrier indices
 enum {
-    B_FULL_KQ = 0, B_EMPTY_KQ = 3, B_FULL_V = 6, B_EMPTY_V = 8, B_GB_FULL = 10, B_GB_EMPTY = 14,
-    B_XREADY = 18, B_XFREE, B_BWU, B_M2DONE, B_WREADY, B_DREADY, B_DELTA, B_SREADY, B_STREADY,
-    B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE
+    B_FULL_KQ = 0, B_EMPTY_KQ = 3, B_FULL_V = 6, B_EMPTY_V = 8, B_GB_FULL = 10, B_GB_EMPTY = 13,
+    B_XREADY0 = 16, B_XREADY1, B_XFREE, B_BWU0, B_BWU1, B_M2DONE0, B_M2DONE1, B_WREADY, B_DREADY, B_DELTA,
+    B_SREADY, B_STREADY, B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE, B_CONV0, B_CONV1
 };
-static_assert(B_DONE < (int)NUM_BARS, "barrier count");
+static_assert(B_CONV1 < (int)NUM_BARS, "barrier count");
 
 // gb slot fields (float offsets)
 constexpr int GB_G = 0, GB_GAM = 64, GB_BET = 128, GB_BG = 192, GB_DEC = 256, GB_QSC = 320, GB_GC = 384;
@@ -112,35 +126,26 @@ __device__ __forceinline__ float2 unh2(uint32_t u) {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
 }
-// One 128-byte tile row (64 values): bf16 in, fp16 out, times f, in place.
-// Rows r..r+7 handled by neighbouring threads start at different 16-byte
-// chunks (c ^ r), so a warp's accesses spread over all banks.
+// One 128-byte tile row (64 values): bf16 in, fp16 out (times f when
+// SCALED), in place. All eight 16-byte loads are issued before any store:
+// the swizzled indices are runtime values, so the compiler could not
+// otherwise move a load above the previous chunk's store.
+template <bool SCALED>
 __device__ __forceinline__ void bf16_row_to_f16(uint8_t* row, uint32_t r, float f) {
     uint4* p = reinterpret_cast<uint4*>(row);
+    uint4 u[8];
+#pragma unroll
+    for (int c0 = 0; c0 < 8; ++c0) u[c0] = p[((uint32_t)c0 ^ r) & 7u];
 #pragma unroll
     for (int c0 = 0; c0 < 8; ++c0) {
-        const uint32_t c = ((uint32_t)c0 ^ r) & 7u;
-        uint4 u = p[c];
-        float2 a = unbf2(u.x), b = unbf2(u.y), d = unbf2(u.z), e = unbf2(u.w);
-        u.x = h2(a.x * f, a.y * f); u.y = h2(b.x * f, b.y * f);
-        u.z = h2(d.x * f, d.y * f); u.w = h2(e.x * f, e.y * f);
-        p[c] = u;
+        float2 a = unbf2(u[c0].x), b = unbf2(u[c0].y), d = unbf2(u[c0].z), e = unbf2(u[c0].w);
+        if (SCALED) {
+            a.x *= f; a.y *= f; b.x *= f; b.y *= f; d.x *= f; d.y *= f; e.x *= f; e.y *= f;
+        }
+        u[c0].x = h2(a.x, a.y); u[c0].y = h2(b.x, b.y); u[c0].z = h2(d.x, d.y); u[c0].w = h2(e.x, e.y);
     }
-}
-// Chunks [c_lo, c_lo + n) (in swizzled visiting order) of one 128-byte row of
-// fp16 values, times f, in place.
-__device__ __forceinline__ void f16_row_scale(uint8_t* row, uint32_t r, float f, int c_lo, int n) {
-    uint4* p = reinterpret_cast<uint4*>(row);
 #pragma unroll
-    for (int c0 = 0; c0 < 8; ++c0) {
-        if (c0 < c_lo || c0 >= c_lo + n) continue;
-        const uint32_t c = ((uint32_t)c0 ^ r) & 7u;
-        uint4 u = p[c];
-        float2 a = unh2(u.x), b = unh2(u.y), d = unh2(u.z), e = unh2(u.w);
-        u.x = h2(a.x * f, a.y * f); u.y = h2(b.x * f, b.y * f);
-        u.z = h2(d.x * f, d.y * f); u.w = h2(e.x * f, e.y * f);
-        p[c] = u;
-    }
+    for (int c0 = 0; c0 < 8; ++c0) p[((uint32_t)c0 ^ r) & 7u] = u[c0];
 }
 // Write 64 floats v[0..63] as fp16 into row `row` of a 128B-swizzled tile.
 __device__ __forceinline__ void store_row_sw128(uint8_t* tile, uint32_t row, const float* v) {
@@ -174,9 +179,16 @@ __device__ unsigned long long* g_trace;
     do {                                                                            \
         if (blockIdx.x == 0 && g_trace && (n) < 128) g_trace[(point) * 128 + (n)] = clock64(); \
     } while (0)
+#define GDN_TRACE_CTA(point)                                                        \
+    do {                                                                            \
+        if (g_trace && blockIdx.x < 128) g_trace[(point) * 128 + blockIdx.x] = globaltimer_ns(); \
+    } while (0)
 #else
 #define GDN_TRACE_AT(point, n) \
     do {                       \
+    } while (0)
+#define GDN_TRACE_CTA(point) \
+    do {                     \
     } while (0)
 #endif
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -197,13 +209,143 @@ __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
     return r != 0;
 }
 
+
+// Off-diagonal blocks of block-row bi (1..3) of T = (I + A)^{-1} (4 x 4
+// blocks of 16 x 16), right-looking: T_ij = -(sum_{k=j+1..bi} T_ik A_kj) T_jj
+// for j = bi-1 .. 0. One warp; T_ik stay in registers as fp16 A fragments,
+// A_kj and T_jj come from shared memory through ldmatrix (fp16 operands, fp32
+// accumulation). Each finished block is written, scaled by the column
+// factors, into Bw = T diag(-beta gamma) and Bu = T diag(beta). The loops run
+// over the largest case (bi = 3) with warp-uniform guards, so that the
+// fragment registers keep compile-time indices and one copy of the code
+// serves all three block-rows.
+__device__ __forceinline__ void solve_block_row(int bi, uint32_t as_u, uint32_t ts_u, uint8_t* bw, uint8_t* bu,
+                                                const float* gb, int lane) {
+    using namespace tc;
+    const int m = lane >> 3, lr = (lane & 7) + 8 * (m & 1), lc8 = m >> 1;
+    auto a_addr = [&](int bk, int bj) {
+        const uint32_t R = (uint32_t)(16 * bk + lr), ch = (uint32_t)(2 * bj + lc8);
+        return as_u + R * 128u + (((ch ^ R) & 7u) << 4);
+    };
+    auto t_addr = [&](int bb) {
+        return ts_u + (uint32_t)bb * 512u + (uint32_t)lr * 32u + (((uint32_t)lc8 ^ ((uint32_t)lr >> 2)) & 1u) * 16u;
+    };
+    const int g = lane >> 2, q = lane & 3;
+    uint32_t Tf[4][4];  // Tf[k] = fragment of T_{bi,k}, k = j+1 .. bi
+#pragma unroll
+    for (int k = 1; k < 4; ++k)
+        if (k == bi) ldsm_x4(t_addr(k), Tf[k]);
+#pragma unroll
+    for (int j = 2; j >= 0; --j) {
+        if (j >= bi) continue;
+        float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = j + 1; k < 4; ++k) {
+            if (k > bi) break;
+            uint32_t b[4];
+            ldsm_x4_t(a_addr(k, j), b);
+            mma16816(y0, Tf[k], b[0], b[1]);
+            mma16816(y1, Tf[k], b[2], b[3]);
+        }
+        const uint32_t ya[4] = {h2(y0[0], y0[1]), h2(y0[2], y0[3]), h2(y1[0], y1[1]), h2(y1[2], y1[3])};
+        uint32_t bt[4];
+        ldsm_x4_t(t_addr(j), bt);
+        float z0[4] = {0.f, 0.f, 0.f, 0.f}, z1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(z0, ya, bt[0], bt[1]);
+        mma16816(z1, ya, bt[2], bt[3]);
+        // T_{bi,j} = -z
+        Tf[j][0] = h2(-z0[0], -z0[1]); Tf[j][1] = h2(-z0[2], -z0[3]);
+        Tf[j][2] = h2(-z1[0], -z1[1]); Tf[j][3] = h2(-z1[2], -z1[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float* z = nt ? z1 : z0;
+            const int S_ = 16 * j + 8 * nt + 2 * q;
+            const float2 fbg = *reinterpret_cast<const float2*>(gb + GB_BG + S_);
+            const float2 fbe = *reinterpret_cast<const float2*>(gb + GB_BET + S_);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t R = (uint32_t)(16 * bi + g + 8 * hh);
+                const uint32_t off = R * 128u + (((((uint32_t)S_ >> 3) ^ R) & 7u) << 4) + (uint32_t)(S_ & 7) * 2u;
+                *reinterpret_cast<uint32_t*>(bw + off) = h2(z[2 * hh] * fbg.x, z[2 * hh + 1] * fbg.y);
+                *reinterpret_cast<uint32_t*>(bu + off) = h2(-z[2 * hh] * fbe.x, -z[2 * hh + 1] * fbe.y);
+            }
+        }
+    }
+}
+
+// A/P pass of one prep group on chunk n (its A and Ad tiles and P buffer
+// n & 1): from X = [K; Q] K^T in TMEM, row r of A (rows 0-63, TMEM lanes
+// 0-63) or of P (lanes 64-127) per thread; gt = the thread's TMEM lane.
+__device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float* gb, int n, int len, float scale,
+                                        int gt) {
+    using namespace tc;
+    const int wq = gt >> 5;
+    const int grp = n & 1;
+    const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
+    uint8_t* As = sm + OFF_AS + (uint32_t)grp * 8192;
+    float* Ad = reinterpret_cast<float*>(sm + OFF_AD + (uint32_t)grp * 4096);
+    // ---- A = strictly-lower(diag(beta) Gamma o K K^T) (fp16 tile + fp32
+    //      diagonal blocks) and P = scale (Gamma o Q K^T) masked r >= s
+    //      (fp16 B tile). Rows 0-31 only have columns 0-31.
+    {
+        const bool isA = wq < 2;
+        const int r = isA ? gt : gt - 64;
+        // beta_r and the output scale enter as exponent offsets (log2 of 0 is -inf: row of zeros)
+        const float base = gb[GB_G + r] + (isA ? lg2(gb[GB_BET + r]) : lg2(scale));
+        // kept columns: s < r (A), s <= r on live rows (P)
+        const int lim = isA ? r : (r < min(C, len - n * C) ? r + 1 : 0);
+        const float4* G4 = reinterpret_cast<const float4*>(gb + GB_G);
+        uint8_t* row = isA ? As + r * 128 : sm + OFF_P + (uint32_t)grp * 8192 + r * 128;
+        const bool wide = (wq & 1) != 0;  // rows 32-63
+#pragma unroll 1
+        for (int hc = 0; hc < 2; ++hc) {  // halves of 32 columns, one TMEM load each
+            if (hc == 1 && !wide) break;
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_base + T_X + 32 * hc, x);
+            tmem_ld_wait();
+            // in place: x[e] becomes the fp32 value of column 32 hc + e
+            const float4* src = G4 + 8 * hc;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 g4 = src[q4];
+                const float gq[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+                for (int e4 = 0; e4 < 4; ++e4) {
+                    const int e = 4 * q4 + e4;
+                    // Gamma_rs = exp(G_r - G_s) <= 1 for s <= r (beta_r / scale folded in)
+                    x[e] = __float_as_uint((32 * hc + e < lim) ? ex2(base - gq[e4]) * __uint_as_float(x[e]) : 0.f);
+                }
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = 4 * hc + c4;
+                uint4 u;
+                u.x = h2(__uint_as_float(x[8 * c4 + 0]), __uint_as_float(x[8 * c4 + 1]));
+                u.y = h2(__uint_as_float(x[8 * c4 + 2]), __uint_as_float(x[8 * c4 + 3]));
+                u.z = h2(__uint_as_float(x[8 * c4 + 4]), __uint_as_float(x[8 * c4 + 5]));
+                u.w = h2(__uint_as_float(x[8 * c4 + 6]), __uint_as_float(x[8 * c4 + 7]));
+                *reinterpret_cast<uint4*>(row + ((((uint32_t)c ^ (uint32_t)r) & 7u) << 4)) = u;
+            }
+            if (isA && ((r >> 5) == hc)) {  // diagonal 16x16 block in fp32, column-major
+                const int h16 = (r >> 4) & 1;
+                float* dcol = Ad + (r >> 4) * 256 + (r & 15);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) dcol[16 * e] = __uint_as_float(h16 ? x[16 + e] : x[e]);
+            }
+        }
+        if (!isA) fence_async_smem();
+    }
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                 const __grid_constant__ CUtensorMap mapV, TcArgs p) {
     using namespace tc;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived by pointer arithmetic (not through an
+    // integer) so that the compiler keeps every access in the shared space
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 4);
@@ -219,16 +361,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const int nc = (len + C - 1) / C;
     const int hk = h / p.grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) GDN_TRACE_CTA(62);
+#ifdef GDN_TRACE
+    if (threadIdx.x == 0 && g_trace && blockIdx.x < 128) {
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        g_trace[61 * 128 + blockIdx.x] = smid;
+    }
+#endif
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < KQ_STAGES; ++i) { mbar_init(&bars[B_FULL_KQ + i], 1); mbar_init(&bars[B_EMPTY_KQ + i], 1); }
         for (int i = 0; i < V_STAGES; ++i) { mbar_init(&bars[B_FULL_V + i], 1); mbar_init(&bars[B_EMPTY_V + i], 1); }
         for (int i = 0; i < GB_SLOTS; ++i) { mbar_init(&bars[B_GB_FULL + i], 1); mbar_init(&bars[B_GB_EMPTY + i], 12); }
-        mbar_init(&bars[B_XREADY], 1); mbar_init(&bars[B_XFREE], 4); mbar_init(&bars[B_BWU], 4);
-        mbar_init(&bars[B_M2DONE], 1); mbar_init(&bars[B_WREADY], 8); mbar_init(&bars[B_DREADY], 1);
-        mbar_init(&bars[B_DELTA], 8); mbar_init(&bars[B_SREADY], 1); mbar_init(&bars[B_STREADY], 8);
-        mbar_init(&bars[B_OREADY], 1); mbar_init(&bars[B_OFREE], 8); mbar_init(&bars[B_PFREE0], 1);
-        mbar_init(&bars[B_PFREE1], 1); mbar_init(&bars[B_DONE], 2);
+        mbar_init(&bars[B_XREADY0], 1); mbar_init(&bars[B_XREADY1], 1); mbar_init(&bars[B_XFREE], 4);
+        mbar_init(&bars[B_BWU0], 4); mbar_init(&bars[B_BWU1], 4);
+        mbar_init(&bars[B_M2DONE0], 1); mbar_init(&bars[B_M2DONE1], 1); mbar_init(&bars[B_WREADY], 4);
+        mbar_init(&bars[B_DREADY], 1); mbar_init(&bars[B_DELTA], 8); mbar_init(&bars[B_SREADY], 1);
+        mbar_init(&bars[B_STREADY], 8); mbar_init(&bars[B_OREADY], 1); mbar_init(&bars[B_OFREE], 8);
+        mbar_init(&bars[B_PFREE0], 1); mbar_init(&bars[B_PFREE1], 1); mbar_init(&bars[B_DONE], 2);
+        mbar_init(&bars[B_CONV0], 8); mbar_init(&bars[B_CONV1], 8);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -236,6 +388,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         tma_prefetch_desc(&mapQ); tma_prefetch_desc(&mapK); tma_prefetch_desc(&mapV);
     }
     if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    // Bw, Bu (both buffers) and P (both buffers) start as zeros: their blocks
+    // above the diagonal are never written afterwards
+    for (uint32_t i = threadIdx.x; i < (3u * 16384u) / 16u; i += NTHREADS)
+        reinterpret_cast<uint4*>(sm + OFF_BW)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -248,12 +405,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     // warp-uniform wait (every lane polls; the warp proceeds only if all saw it)
     auto WAITW = [&](int b, uint32_t parity) { return __all_sync(0xffffffffu, WAIT(b, parity)) != 0; };
 
+    // Roles (20 warps). Each role's register budget is set at the top of its
+    // own branch, so that the compiler allocates that role's code within it.
+    //   warp 0        TMA producer (K, Q, V tiles; L2 prefetch 3 chunks ahead)
+    //   warp 1        state-dependent products M3a, M3b, M5, M4; owns TMEM
+    //   warp 2        look-ahead products M1, M2
+    //   warp 3        g, beta -> cumulative decay and factors per chunk
+    //   warps 4-7     prep group 0 (even chunks), warps 8-11 group 1 (odd):
+    //                 A/P, triangular solve, -W^T hand-off
+    //   warps 12-19   state: thread (j, half) holds half of column j of S (fp32);
+    //                 between chunks, the bf16 -> fp16 operands two chunks ahead
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
+        regs_dec<REGS_ROLES>();
         if (lane == 0) {
             int issued_kq = 0, issued_v = 0;
             for (int n = 0; n < nc && !*abort_flag; ++n) {
                 const int t = (int)(t0 + (long long)n * C);
+                if (n + 3 < nc) {  // warm L2 for chunk n + 3 (its stage is still in use)
+                    const int tp = t + 3 * C;
+                    tma_prefetch_l2_3d(&mapK, 0, hk, tp); tma_prefetch_l2_3d(&mapK, 64, hk, tp);
+                    tma_prefetch_l2_3d(&mapQ, 0, hk, tp); tma_prefetch_l2_3d(&mapQ, 64, hk, tp);
+                    tma_prefetch_l2_3d(&mapV, 0, h, tp); tma_prefetch_l2_3d(&mapV, 64, h, tp);
+                }
                 const int s = n % KQ_STAGES;
                 if (n >= KQ_STAGES && !WAIT(B_EMPTY_KQ + s, ((n / KQ_STAGES) - 1) & 1)) break;
                 uint8_t* kq = kq_tile(n);
@@ -275,12 +449,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             // never leave with copies in flight: wait for the last loads of each
             // ring (they land whether or not anyone consumed them; no abort check)
             for (int n = issued_kq - 1; n >= 0 && n >= issued_kq - KQ_STAGES; --n)
-                mbar_wait(&bars[B_FULL_KQ + n % KQ_STAGES], (n / KQ_STAGES) & 1, nullptr, 200000000ull);
+                mbar_wait(&bars[B_FULL_KQ + n % KQ_STAGES], (n / KQ_STAGES) & 1, nullptr, 10000u);
             for (int n = issued_v - 1; n >= 0 && n >= issued_v - V_STAGES; --n)
-                mbar_wait(&bars[B_FULL_V + n % V_STAGES], (n / V_STAGES) & 1, nullptr, 200000000ull);
+                mbar_wait(&bars[B_FULL_V + n % V_STAGES], (n / V_STAGES) & 1, nullptr, 10000u);
         }
     } else if (warp == 1) {
         // -------------------------------------------- state-dependent products
+        regs_dec<REGS_ROLES>();
         if (lane == 0) {
             const uint32_t id_n64_mn = idesc_f16(128, 64, false, true);
             const uint32_t id_n64_k = idesc_f16(128, 64, false, false);
@@ -291,6 +466,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 GDN_TRACE_AT(20, n);
                 tc_fence_after();
                 // M3a: D^T = U^T + S^T (-W)^T  (accumulates onto U^T written by M2)
+#pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + T_DU, tmem + T_ST + 8 * kk, sdesc_sw128(wt + kk * 2048, 16384, 1024), id_n64_mn, 1u);
                 mma_commit(&bars[B_DREADY]);
@@ -298,6 +474,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 tc_fence_after();
                 // M3b: O^T = S^T (gamma scale Q)^T
                 const uint32_t kq = smem_u32(kq_tile(n));
+#pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + T_O, tmem + T_ST + 8 * kk,
                                 sdesc_sw128(kq + 8192 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024), id_n64_k,
@@ -305,13 +482,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!WAIT(B_DELTA, n & 1)) break;
                 GDN_TRACE_AT(21, n);
                 tc_fence_after();
-                // M5: Sacc = D^T Kdec
+                // M5: Sacc = (D^T diag(Gamma_last,.)) K
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ts(tmem + T_SACC, tmem + T_DT + 8 * kk, sdesc_sw128(kq + kk * 2048, 16384, 1024),
+                    mma_bf16_ts(tmem + T_SACC, tmem + T_DTD + 8 * kk, sdesc_sw128(kq + kk * 2048, 16384, 1024),
                                 id_n128_mn, kk > 0 ? 1u : 0u);
                 mma_commit(&bars[B_SREADY]);
                 // M4: O^T += D^T P^T
                 const uint32_t pt = smem_u32(sm + OFF_P + (uint32_t)(n & 1) * 8192);
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16_ts(tmem + T_O, tmem + T_DT + 8 * kk, sdesc_sw128(pt + kk * 32, 16, 1024), id_n64_k, 1u);
                 mma_commit(&bars[B_OREADY]);
@@ -322,69 +501,67 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else if (warp == 2) {
         // ------------------------------------------------- look-ahead products
+        // Issue order M1(0), then per chunk m: M1(m+1), M2(m). M1(m+1) needs the
+        // stage and X released by the prep group of m (A/P done); M2(m) needs
+        // the prep group of m done (T: BWU), chunk m converted (fp16 K, V:
+        // CONV) and the U and W regions released by chunk m-1. The state warps
+        // wait for M1(c) before converting chunk c; the next phase of that
+        // XREADY barrier is M1(c+2), which this order issues after M2(c), i.e.
+        // after conversion c was seen.
+        regs_dec<REGS_ROLES>();
         if (lane == 0) {
             const uint32_t id_x = idesc_bf16(128, 64, false, false);  // raw bf16 K, Q
             const uint32_t id_wu = idesc_f16(128, 64, true, false);
             auto issue_m1 = [&](int n) {
                 const uint32_t kq = smem_u32(kq_tile(n));
+#pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
                     mma_bf16(tmem + T_X, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), id_x,
                              kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&bars[B_XREADY]);
+                mma_commit(&bars[B_XREADY0 + (n & 1)]);
             };
             auto issue_m2 = [&](int n) {
                 const uint32_t kq = smem_u32(kq_tile(n)), vt = smem_u32(v_tile(n));
-                const uint32_t bw = smem_u32(sm + OFF_BW), bu = smem_u32(sm + OFF_BU);
+                const uint32_t bw = smem_u32(sm + OFF_BW + (uint32_t)(n & 1) * 8192);
+                const uint32_t bu = smem_u32(sm + OFF_BU + (uint32_t)(n & 1) * 8192);
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + T_W, sdesc_sw128(kq + kk * 2048, 16384, 1024), sdesc_sw128(bw + kk * 32, 16, 1024),
                              id_wu, kk > 0 ? 1u : 0u);
+#pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + T_DU, sdesc_sw128(vt + kk * 2048, 8192, 1024), sdesc_sw128(bu + kk * 32, 16, 1024),
                              id_wu, kk > 0 ? 1u : 0u);
-                mma_commit(&bars[B_M2DONE]);
+                mma_commit(&bars[B_M2DONE0 + (n & 1)]);
                 mma_commit(&bars[B_EMPTY_V + n % V_STAGES]);
             };
-            // Issue whichever product is ready: M1(m1) once X of chunk m1-1 is
-            // consumed and the stage has landed; M2(m2) once T of chunk m2 is
-            // ready and the state warps released the U and W regions of chunk
-            // m2-1. Polls back off with nanosleep so that this thread does not
-            // take issue slots from the warps sharing its scheduler.
             if (nc > 0 && WAIT(B_FULL_KQ, 0)) {
                 tc_fence_after();
                 GDN_TRACE_AT(30, 0);
                 issue_m1(0);
-                int m1 = 1, m2 = 0;
-                uint64_t t_last = globaltimer_ns();
-                while (m2 < nc && !*abort_flag) {
-                    bool progress = false;
-                    if (m1 < nc && m1 <= m2 + 1 && mbar_test(&bars[B_FULL_KQ + m1 % KQ_STAGES], (m1 / KQ_STAGES) & 1) &&
-                        mbar_test(&bars[B_XFREE], (m1 - 1) & 1)) {
+                for (int m = 0; m < nc; ++m) {
+                    if (m + 1 < nc) {
+                        if (!WAIT(B_FULL_KQ + (m + 1) % KQ_STAGES, ((m + 1) / KQ_STAGES) & 1) ||
+                            !WAIT(B_XFREE, m & 1))
+                            break;
                         tc_fence_after();
-                        GDN_TRACE_AT(30, m1);
-                        issue_m1(m1++);
-                        progress = true;
+                        GDN_TRACE_AT(30, m + 1);
+                        issue_m1(m + 1);
                     }
-                    if (mbar_test(&bars[B_BWU], m2 & 1) && mbar_test(&bars[B_FULL_V + m2 % V_STAGES], (m2 / V_STAGES) & 1) &&
-                        (m2 == 0 || (mbar_test(&bars[B_WREADY], (m2 - 1) & 1) && mbar_test(&bars[B_DELTA], (m2 - 1) & 1)))) {
-                        tc_fence_after();
-                        GDN_TRACE_AT(31, m2);
-                        issue_m2(m2++);
-                        progress = true;
-                    }
-                    if (progress) {
-                        t_last = globaltimer_ns();
-                    } else {
-                        __nanosleep(40);
-                        if (globaltimer_ns() - t_last > 2000000000ull) *abort_flag = 1;
-                    }
+                    if (!WAIT(B_CONV0 + (m & 1), (m >> 1) & 1) || !WAIT(B_BWU0 + (m & 1), (m >> 1) & 1)) break;
+                    if (m >= 1 && (!WAIT(B_DELTA, (m - 1) & 1) || !WAIT(B_WREADY, (m - 1) & 1))) break;
+                    tc_fence_after();
+                    GDN_TRACE_AT(31, m);
+                    issue_m2(m);
                 }
             }
             mma_commit(&bars[B_DONE]);
         }
     } else if (warp == 3) {
         // ------------------------------------- g, beta -> decay factors per chunk
+        regs_dec<REGS_ROLES>();
         for (int n = 0; n < nc; ++n) {
             const int slot = n % GB_SLOTS;
             if (n >= GB_SLOTS && !WAITW(B_GB_EMPTY + slot, ((n / GB_SLOTS) - 1) & 1)) break;
@@ -421,282 +598,263 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (lane == 0) mbar_arrive(&bars[B_GB_FULL + slot]);
             if (lane == 0) GDN_TRACE_AT(41, n);
         }
-    } else if (warp < 8) {
-        // ----------------------------------------------------------------- prep
-        const int pt = threadIdx.x - 128;  // 0..127 = TMEM lane
-        const int wq = warp - 4;           // lane quadrant
-        float* Am = reinterpret_cast<float*>(sm + OFF_A);
-        float* Tm = reinterpret_cast<float*>(sm + OFF_T);
-        const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-        for (int n = 0; n < nc; ++n) {
+    } else if (warp < 12) {
+        // ---------------------------------------------------------- prep groups
+        // group g = 0 (warps 4-7) takes the even chunks, g = 1 (warps 8-11) the
+        // odd ones; each owns the A, Ad, Ts tiles, Bw/Bu and P buffers g
+        regs_dec<REGS_PREP>();
+        const int g = (warp - 4) >> 2;
+        const int gt = threadIdx.x - 128 - 128 * g;  // 0..127 = TMEM lane
+        const int wq = gt >> 5;
+        const int bar_id = 1 + g;
+        uint8_t* As = sm + OFF_AS + (uint32_t)g * 8192;
+        float* Ad = reinterpret_cast<float*>(sm + OFF_AD + (uint32_t)g * 4096);
+        uint8_t* Ts = sm + OFF_TS + (uint32_t)g * 2048;
+        uint8_t* bw = sm + OFF_BW + (uint32_t)g * 8192;
+        uint8_t* bu = sm + OFF_BU + (uint32_t)g * 8192;
+        for (int n = g; n < nc; n += 2) {
             const float* gb = gb_slot(n);
-            // the stage's TMA completion is observed here too: the prep threads
-            // rescale Q and K in place with ordinary loads and stores
-            bool ok = WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1) &&
-                      WAITW(B_FULL_KQ + n % KQ_STAGES, (n / KQ_STAGES) & 1) &&
-                      WAITW(B_FULL_V + n % V_STAGES, (n / V_STAGES) & 1) && WAITW(B_XREADY, n & 1);
-            if (ok && wq >= 2 && n >= 2) ok = WAITW(B_PFREE0 + (n & 1), ((n >> 1) - 1) & 1);
-            if (named_sync_or(1, 128, !ok)) break;
-            if (pt == 0) GDN_TRACE_AT(0, n);
+            const uint32_t ph = (uint32_t)(n >> 1) & 1u;  // phase parity of this group's barriers
+            bool ok = WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1) && WAITW(B_XREADY0 + g, ph);
+            // P and Bw/Bu buffers g were last read by the products of chunk n - 2
+            if (ok && wq >= 2 && n >= 2) ok = WAITW(B_PFREE0 + g, ph ^ 1u);
+            if (ok && n >= 2) ok = WAITW(B_M2DONE0 + g, ph ^ 1u);
+            if (named_sync_or(bar_id, 128, !ok)) break;
+            if (gt == 0) GDN_TRACE_AT(0, n);
             tc_fence_after();
-            {
-                uint32_t x[64];
-                tmem_ld32(tmem + lane_base + T_X, *reinterpret_cast<uint32_t(*)[32]>(x));
-                tmem_ld32(tmem + lane_base + T_X + 32, *reinterpret_cast<uint32_t(*)[32]>(x + 32));
-                tmem_ld_wait();
-                if (wq < 2) {  // rows of K K^T -> A (fp32)
-                    const int r = pt;
-                    const float Gr = gb[GB_G + r], br = gb[GB_BET + r];
-                    float* arow = Am + r * LDA;
-#pragma unroll
-                    for (int s4 = 0; s4 < 64; s4 += 4) {
-                        float4 a;
-                        a.x = (s4 + 0 < r) ? br * ex2(Gr - gb[GB_G + s4 + 0]) * __uint_as_float(x[s4 + 0]) : 0.f;
-                        a.y = (s4 + 1 < r) ? br * ex2(Gr - gb[GB_G + s4 + 1]) * __uint_as_float(x[s4 + 1]) : 0.f;
-                        a.z = (s4 + 2 < r) ? br * ex2(Gr - gb[GB_G + s4 + 2]) * __uint_as_float(x[s4 + 2]) : 0.f;
-                        a.w = (s4 + 3 < r) ? br * ex2(Gr - gb[GB_G + s4 + 3]) * __uint_as_float(x[s4 + 3]) : 0.f;
-                        *reinterpret_cast<float4*>(arow + s4) = a;
-                    }
-                } else {  // rows of Q K^T -> P (bf16, decayed, causal, scaled)
-                    const int r = pt - 64;
-                    const float Gr = gb[GB_G + r];
-                    const bool live = r < min(C, len - n * C);
-                    float pv[64];
-#pragma unroll
-                    for (int s = 0; s < 64; ++s)
-                        pv[s] = (live && s <= r) ? p.scale * ex2(Gr - gb[GB_G + s]) * __uint_as_float(x[s]) : 0.f;
-                    store_row_sw128(sm + OFF_P + (uint32_t)(n & 1) * 8192, (uint32_t)r, pv);
-                    fence_async_smem();
-                }
-            }
+            ap_pass(sm, tmem, gb, n, len, p.scale, gt);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_XFREE]);
-            // ---- fp16 operands: K, V as they are, Q times gamma scale (M1 has
-            //      consumed the bf16 K and Q of this chunk)
-            {
-                const int r = pt & 63, kb = pt >> 6;
-                uint8_t* kq = kq_tile(n) + (uint32_t)kb * 16384 + (uint32_t)r * 128;
-                bf16_row_to_f16(kq, r, 1.f);
-                bf16_row_to_f16(kq + 8192, r, gb[GB_QSC + r]);
-                bf16_row_to_f16(v_tile(n) + (uint32_t)kb * 8192 + (uint32_t)r * 128, r, 1.f);
-            }
-            if (pt == 0) GDN_TRACE_AT(1, n);
-            named_sync(1, 128);
-            // ---- T = (I + A)^{-1}: 16x16 diagonal blocks by substitution, then
-            //      off-diagonal blocks level by level: T_ij = -T_ii sum_k A_ik T_kj
-            if (pt < 64) {
-                const int b = pt >> 4, c = pt & 15;
+            if (gt == 0) GDN_TRACE_AT(1, n);
+            named_sync(bar_id, 128);
+            // ---- diagonal blocks T_bb = (I + A_bb)^{-1}, one per warp, by forward
+            //      substitution in fp32 (lane c < 16 solves column c); written to Ts
+            //      (fp16) and, scaled, to the diagonal blocks of Bw and Bu
+            if (lane < 16) {
+                const int b = wq, c = lane;
+                // right-looking: once x_ss is final, subtract its column from the rest
                 float xs[16];
 #pragma unroll
+                for (int rr = 0; rr < 16; ++rr) xs[rr] = (rr == c) ? 1.f : 0.f;
+                const float4* acol = reinterpret_cast<const float4*>(Ad + b * 256);
+#pragma unroll
+                for (int ss = 0; ss < 15; ++ss) {
+#pragma unroll
+                    for (int q4 = (ss + 1) >> 2; q4 < 4; ++q4) {
+                        const float4 a4 = acol[ss * 4 + q4];
+                        if (4 * q4 + 0 > ss) xs[4 * q4 + 0] = fmaf(-a4.x, xs[ss], xs[4 * q4 + 0]);
+                        if (4 * q4 + 1 > ss) xs[4 * q4 + 1] = fmaf(-a4.y, xs[ss], xs[4 * q4 + 1]);
+                        if (4 * q4 + 2 > ss) xs[4 * q4 + 2] = fmaf(-a4.z, xs[ss], xs[4 * q4 + 2]);
+                        if (4 * q4 + 3 > ss) xs[4 * q4 + 3] = fmaf(-a4.w, xs[ss], xs[4 * q4 + 3]);
+                    }
+                }
+                const int S_ = 16 * b + c;
+                const float fw = -gb[GB_BG + S_], fu = gb[GB_BET + S_];
+#pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
-                    float acc = (rr == c) ? 1.f : 0.f;
-                    const float* arow = Am + (16 * b + rr) * LDA + 16 * b;
-#pragma unroll
-                    for (int ss = 0; ss < rr; ++ss) acc = fmaf(-arow[ss], xs[ss], acc);
-                    xs[rr] = acc;
+                    const uint32_t R = (uint32_t)(16 * b + rr);
+                    *reinterpret_cast<__half*>(Ts + b * 512 + rr * 32 + ((((uint32_t)c >> 3) ^ ((uint32_t)rr >> 2)) & 1u) * 16 +
+                                               (c & 7) * 2) = __float2half_rn(xs[rr]);
+                    const uint32_t off = R * 128u + (((((uint32_t)S_ >> 3) ^ R) & 7u) << 4) + (uint32_t)(S_ & 7) * 2u;
+                    *reinterpret_cast<__half*>(bw + off) = __float2half_rn(xs[rr] * fw);
+                    *reinterpret_cast<__half*>(bu + off) = __float2half_rn(xs[rr] * fu);
                 }
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) Tm[(16 * b + rr) * LDA + 16 * b + c] = xs[rr];
             }
-            named_sync(1, 128);
-#pragma unroll
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                float y[6];
-#pragma unroll
-                for (int t = 0; t < 6; ++t) {
-                    y[t] = 0.f;
-                    if (t < 2 * nb) {
-                        const int e = pt + 128 * t, j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-                        float acc = 0.f;
-                        for (int kb = j; kb < i; ++kb) {
-                            const float* arow = Am + (16 * i + r) * LDA + 16 * kb;
-                            const float* tcol = Tm + (16 * kb) * LDA + 16 * j + c;
-#pragma unroll
-                            for (int m = 0; m < 16; ++m) acc = fmaf(arow[m], tcol[m * LDA], acc);
-                        }
-                        y[t] = acc;
-                    }
-                }
-                named_sync(1, 128);
-#pragma unroll
-                for (int t = 0; t < 6; ++t)
-                    if (t < 2 * nb) {
-                        const int e = pt + 128 * t, j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-                        Tm[(16 * i + r) * LDA + 16 * j + c] = y[t];
-                    }
-                named_sync(1, 128);
-#pragma unroll
-                for (int t = 0; t < 6; ++t)
-                    if (t < 2 * nb) {
-                        const int e = pt + 128 * t, j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-                        const float* trow = Tm + (16 * i + r) * LDA + 16 * i;
-                        const float* ycol = Tm + (16 * i) * LDA + 16 * j + c;
-                        float acc = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) acc = fmaf(trow[m], ycol[m * LDA], acc);
-                        y[t] = -acc;
-                    }
-                named_sync(1, 128);
-#pragma unroll
-                for (int t = 0; t < 6; ++t)
-                    if (t < 2 * nb) {
-                        const int e = pt + 128 * t, j = e >> 8, r = (e >> 4) & 15, c = e & 15, i = j + d;
-                        Tm[(16 * i + r) * LDA + 16 * j + c] = y[t];
-                    }
-                named_sync(1, 128);
-            }
-            if (pt == 0) GDN_TRACE_AT(5, n);
-            // ---- Bw = T diag(beta gamma), Bu = T diag(beta) (fp16, K-major B
-            //      tiles); the previous chunk's M2 must have read them
-            ok = n < 1 || WAITW(B_M2DONE, (n - 1) & 1);
-            if (named_sync_or(1, 128, !ok)) break;
-            {
-                const int r = pt & 63;
-                const float* f = gb + ((pt < 64) ? GB_BG : GB_BET);
-                const float* trow = Tm + r * LDA;
-                float v[64];
-#pragma unroll
-                for (int s = 0; s < 64; ++s) v[s] = (s <= r) ? trow[s] * f[s] : 0.f;
-                store_row_sw128(sm + ((pt < 64) ? OFF_BW : OFF_BU), (uint32_t)r, v);
-            }
+            if (gt == 0) GDN_TRACE_AT(2, n);
+            named_sync(bar_id, 128);
+            // ---- off-diagonal blocks, block-row i = wq by warp wq (right-looking:
+            //      T_ij = -(sum_{k=j+1..i} T_ik A_kj) T_jj), on the warp MMA
+            if (wq >= 1) solve_block_row(wq, smem_u32(As), smem_u32(Ts), bw, bu, gb, lane);
+            if (lane == 0) GDN_TRACE_AT(56 + wq, n);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&bars[B_BWU]);
+                mbar_arrive(&bars[B_BWU0 + g]);
                 mbar_arrive(&bars[B_GB_EMPTY + n % GB_SLOTS]);
             }
-            if (pt == 0) GDN_TRACE_AT(2, n);
+            if (gt == 0) GDN_TRACE_AT(4, n);
+            // ---- -W^T of chunk n from TMEM (lane = key index i = gt, columns =
+            //      chunk rows r) into the MN-major fp16 B tile of M3a, once M2(n)
+            //      has run and M3a(n-1) has finished reading the tile
+            ok = WAITW(B_M2DONE0 + g, ph) && (n < 1 || WAITW(B_DREADY, (n - 1) & 1));
+            if (named_sync_or(bar_id, 128, !ok)) break;
+            tc_fence_after();
+            {
+                const uint32_t lb = (uint32_t)(32 * wq) << 16;
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    uint32_t w[32];
+                    tmem_ld32(tmem + lb + T_W + 32 * hq, w);
+                    tmem_ld_wait();
+                    store_half_row_sw128(sm + OFF_WT, (uint32_t)gt, reinterpret_cast<const float*>(w), hq);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_WREADY]);
+            if (gt == 0) GDN_TRACE_AT(13, n);
         }
     } else {
         // ---------------------------------------------------------------- state
-        const int ws = warp - 8, q4 = ws & 3, hf = ws >> 2;
+        // warps 12-19: thread (j, hf) holds rows 64 hf .. 64 hf + 63 of column j
+        // of S in fp32 for the whole sequence; handles chunk rows 32 hf .. + 31
+        // of Delta^T and of the output
+        regs_inc<REGS_STATE>();
+        const int ws = warp - 12, q4 = warp & 3, hf = ws >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const size_t sbase = ((size_t)n_seq * p.h_v + h) * (size_t)(D * D);
         float S[64];
+        if (p.h0) {
+            const float* hp = p.h0 + sbase + (size_t)(64 * hf) * D + j;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) S[c] = p.h0 ? p.h0[sbase + (size_t)(64 * hf + c) * D + j] : 0.f;
+            for (int c = 0; c < 64; ++c) S[c] = hp[c * D];
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) S[c] = 0.f;
+        }
         auto put_state_f16 = [&]() {
-            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = h2(S[2 * c], S[2 * c + 1]);
-            tmem_st32(tmem + lane_base + T_ST + 32 * hf, pk);
+            for (int q = 0; q < 2; ++q) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pk[c] = h2(S[32 * q + 2 * c], S[32 * q + 2 * c + 1]);
+                tmem_st16(tmem + lane_base + T_ST + 32 * hf + 16 * q, pk);
+            }
             tmem_st_wait();
         };
         put_state_f16();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_STREADY]);
-        TOut* o = static_cast<TOut*>(p.o);
-        const int tid_s = ws * 32 + lane;  // 0..255
-        // -W^T and Kdec of chunk m, once M2(m) has run: -W^T from TMEM (lane =
-        // key index i, columns = chunk rows r) into the MN-major fp16 B tile;
-        // K rows of the stage scaled by Gamma_last,r in place.
-        auto produce_w = [&](int m) -> bool {
-            if (!WAITW(B_GB_FULL + m % GB_SLOTS, (m / GB_SLOTS) & 1) || !WAITW(B_M2DONE, m & 1)) return false;
-            tc_fence_after();
-            {
-                uint32_t w[32];
-                tmem_ld32(tmem + lane_base + T_W + 32 * hf, w);
-                tmem_ld_wait();
-                float v[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) v[c] = -__uint_as_float(w[c]);
-                store_half_row_sw128(sm + OFF_WT, (uint32_t)j, v, hf);
-            }
-            {
-                const int r = tid_s & 63, kb = (tid_s >> 6) & 1, half = tid_s >> 7;
-                f16_row_scale(kq_tile(m) + (uint32_t)kb * 16384 + (uint32_t)r * 128, (uint32_t)r,
-                              gb_slot(m)[GB_DEC + r], 4 * half, 4);
+        // bf16 -> fp16 operands of chunk m, in place (K as it is and Q times
+        // gamma scale once M1(m) has consumed the bf16 K and Q; V as it is):
+        // 3 tiles x 128 row halves of 64 values over the 256 state threads
+        const int ts = 32 * ws + lane;
+        auto convert = [&](int m) -> bool {
+            if (!WAITW(B_GB_FULL + m % GB_SLOTS, (m / GB_SLOTS) & 1) ||
+                !WAITW(B_XREADY0 + (m & 1), (m >> 1) & 1) || !WAITW(B_FULL_V + m % V_STAGES, (m / V_STAGES) & 1))
+                return false;
+            const float* gbm = gb_slot(m);
+#pragma unroll 1
+            for (int item = ts; item < 384; item += 256) {
+                const int t = item >> 7, rh = item & 127, r = rh & 63, kb = rh >> 6;
+                uint8_t* row = t == 2 ? v_tile(m) + (uint32_t)kb * 8192 + (uint32_t)r * 128
+                                      : kq_tile(m) + (uint32_t)kb * 16384 + (uint32_t)t * 8192 + (uint32_t)r * 128;
+                bf16_row_to_f16<true>(row, (uint32_t)r, t == 1 ? gbm[GB_QSC + r] : 1.f);
             }
             fence_async_smem();
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_WREADY]);
-            if (ws == 0 && lane == 0) GDN_TRACE_AT(13, m);
+            if (lane == 0) mbar_arrive(&bars[B_CONV0 + (m & 1)]);
             return true;
         };
-        bool alive = nc == 0 || produce_w(0);
-        for (int n = 0; n < nc && alive; ++n) {
-            // Delta^T (fp32, TMEM) -> fp16 A operand
-            if (!WAITW(B_DREADY, n & 1)) break;
-            if (ws == 0 && lane == 0) GDN_TRACE_AT(10, n);
-            tc_fence_after();
-            {
-                uint32_t dr[32], pk[16];
-                tmem_ld32(tmem + lane_base + T_DU + 32 * hf, dr);
-                tmem_ld_wait();
+        TOut* o = static_cast<TOut*>(p.o);
+        // conversions run two chunks ahead of the state: chunk n + 2 after the
+        // output of chunk n (iterations n = -2, -1 only convert chunks 0, 1);
+        // one call site keeps a single copy of the conversion code
+        for (int n = -2; n < nc; ++n) {
+            if (n >= 0) {
+                if (!WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1)) break;
+                const float* gb = gb_slot(n);
+                // Delta^T (fp32, TMEM) -> fp16 A operands: as is (for M4) and scaled
+                // by Gamma_last,r (for M5); one TMEM load (a TMEM round trip costs
+                // about 200 cycles while the tensor core is busy)
+                if (!WAITW(B_DREADY, n & 1)) break;
+                if (ws == 0 && lane == 0) GDN_TRACE_AT(10, n);
+                tc_fence_after();
+                {
+                    // both halves loaded before the single wait
+                    uint32_t dr0[16], dr1[16];
+                    tmem_ld16(tmem + lane_base + T_DU + 32 * hf, dr0);
+                    tmem_ld16(tmem + lane_base + T_DU + 32 * hf + 16, dr1);
+                    tmem_ld_wait();
+                    const float4* dec4 = reinterpret_cast<const float4*>(gb + GB_DEC + 32 * hf);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) pk[c] = h2(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1]));
-                tmem_st16(tmem + lane_base + T_DT + 16 * hf, pk);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t* dr = hh ? dr1 : dr0;
+                        uint32_t pk[8], pd[8];
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const float4 d4 = dec4[4 * hh + c4];
+                            const float a0 = __uint_as_float(dr[4 * c4]), a1 = __uint_as_float(dr[4 * c4 + 1]);
+                            const float a2 = __uint_as_float(dr[4 * c4 + 2]), a3 = __uint_as_float(dr[4 * c4 + 3]);
+                            pk[2 * c4] = h2(a0, a1); pk[2 * c4 + 1] = h2(a2, a3);
+                            pd[2 * c4] = h2(a0 * d4.x, a1 * d4.y); pd[2 * c4 + 1] = h2(a2 * d4.z, a3 * d4.w);
+                        }
+                        tmem_st8(tmem + lane_base + T_DTD + 16 * hf + 8 * hh, pd);
+                        tmem_st8(tmem + lane_base + T_DT + 16 * hf + 8 * hh, pk);
+                    }
+                }
                 tmem_st_wait();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_DELTA]);
-            // next chunk's -W^T and Kdec while M5 of this chunk runs (M3a(n)
-            // has finished reading -W^T(n): it completed before DREADY(n))
-            if (n + 1 < nc && !produce_w(n + 1)) break;
-            // state update S^T <- gamma_last S^T + Delta^T Kdec
-            if (!WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1)) break;
-            const float gC = gb_slot(n)[GB_GC];
-            if (!WAITW(B_SREADY, n & 1)) break;
-            if (ws == 0 && lane == 0) GDN_TRACE_AT(11, n);
-            tc_fence_after();
-            {
-                uint32_t acc[32];
-                tmem_ld32(tmem + lane_base + T_SACC + 64 * hf, acc);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], __uint_as_float(acc[c]));
-                tmem_ld32(tmem + lane_base + T_SACC + 64 * hf + 32, acc);
-                tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gC, S[32 + c], __uint_as_float(acc[c]));
-            }
-            put_state_f16();
-            tc_fence_before();
-            __syncwarp();
-            if (ws == 0 && lane == 0) GDN_TRACE_AT(12, n);
-            if (lane == 0) {
-                mbar_arrive(&bars[B_STREADY]);
-                mbar_arrive(&bars[B_GB_EMPTY + n % GB_SLOTS]);
-            }
-            // output rows r = 32 hf .. 32 hf + 31 of this chunk
-            if (!WAITW(B_OREADY, n & 1)) break;
-            tc_fence_after();
-            {
-                uint32_t ov[32];
-                tmem_ld32(tmem + lane_base + T_O + 32 * hf, ov);
-                tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_OFREE]);
-                const int L = min(C, len - n * C);
-                const long long tb = t0 + (long long)n * C + 32 * hf;
+                if (lane == 0) mbar_arrive(&bars[B_DELTA]);
+                // state update S^T <- gamma_last S^T + Delta^T Kdec
+                const float gC = gb[GB_GC];
+                if (!WAITW(B_SREADY, n & 1)) break;
+                if (ws == 0 && lane == 0) GDN_TRACE_AT(11, n);
+                tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (32 * hf + c < L)
-                        o[((size_t)(tb + c) * p.h_v + h) * D + j] = from_f32<TOut>(__uint_as_float(ov[c]));
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t acc[32];
+                    tmem_ld32(tmem + lane_base + T_SACC + 64 * hf + 32 * q, acc);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) S[32 * q + c] = fmaf(gC, S[32 * q + c], __uint_as_float(acc[c]));
+                }
+                put_state_f16();
+                tc_fence_before();
+                __syncwarp();
+                if (ws == 0 && lane == 0) GDN_TRACE_AT(12, n);
+                if (lane == 0) {
+                    mbar_arrive(&bars[B_STREADY]);
+                    mbar_arrive(&bars[B_GB_EMPTY + n % GB_SLOTS]);
+                }
+                // output rows 32 hf .. 32 hf + 31 of this chunk
+                if (!WAITW(B_OREADY, n & 1)) break;
+                tc_fence_after();
+                {
+                    // o[t0 + n C + r][h][j] for r < nv: one row per register; a byte
+                    // pointer stepped by the token stride (the full-chunk case has no
+                    // per-row test)
+                    const int nv = min(C, len - n * C) - 32 * hf;  // valid rows of this half
+                    char* orow = reinterpret_cast<char*>(o + ((size_t)(t0 + (long long)n * C + 32 * hf) * p.h_v + h) * D + j);
+                    const size_t ostep = (size_t)p.h_v * D * sizeof(TOut);
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + lane_base + T_O + 32 * hf, ov);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[B_OFREE]);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (c < nv) *reinterpret_cast<TOut*>(orow) = from_f32<TOut>(__uint_as_float(ov[c]));
+                        orow += ostep;
+                    }
+                }
             }
+            if (n + 2 < nc && !convert(n + 2)) break;
+            if (n >= 0 && ws == 0 && lane == 0) GDN_TRACE_AT(14, n);
         }
         if (p.hT && !*abort_flag) {
+            float* hp = p.hT + sbase + (size_t)(64 * hf) * D + j;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) p.hT[sbase + (size_t)(64 * hf + c) * D + j] = S[c];
+            for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
         }
     }
 
     // ---- teardown: every product finished, then free TMEM
     __syncthreads();
     if (warp == 1) {
-        mbar_wait(&bars[B_DONE], 0, nullptr, 200000000ull);
+        mbar_wait(&bars[B_DONE], 0, nullptr, 10000u);
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag) set_device_error(2u);
+    if (threadIdx.x == 0) GDN_TRACE_CTA(63);
 }
 
 }  // namespace tck

@@ -184,4 +184,12 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     return launch_simt<float, float>(a, smem, s);
 }
 
+#ifdef GDN_TRACE
+// Instrumented builds only (not part of the ABI): device buffer of 64 x 128
+// clock64 stamps that the prefill kernel's block 0 fills per role and chunk.
+int gdn_debug_set_trace(unsigned long long* buf) {
+    return cudaMemcpyToSymbol(gdn::tck::g_trace, &buf, sizeof buf) == cudaSuccess ? 0 : 3;
+}
+#endif
+
 }  // extern "C"

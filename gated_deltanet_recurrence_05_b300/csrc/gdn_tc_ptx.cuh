@@ -76,24 +76,34 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
     return ok != 0;
 }
 
-// Bounded wait for phase `parity` of `bar`. Gives up (returns false) after
-// `limit_ns` of wall time or 2^24 polls, or as soon as *abort becomes nonzero.
-// On a timeout it raises *abort so that every other waiter also gives up.
-// `abort` may be null (teardown waits that must not be cut short by an abort).
-// Waiting threads sleep in try_wait (suspend hint) and back off with
-// nanosleep, so they leave issue slots to the warps that do work.
+// Bounded wait for phase `parity` of `bar`. Each try_wait may suspend the
+// thread for up to `hint_ns` until the phase completes (the hardware wakes it
+// at completion), so waiting costs no issue slots. Gives up (returns false)
+// after `max_polls` polls (about max_polls x hint_ns of wall time at most), or
+// as soon as *abort becomes nonzero; on giving up it raises *abort so that
+// every other waiter also gives up. `abort` may be null (teardown waits that
+// must not be cut short by an abort). The loop is kept small: it is inlined at
+// every wait site and the kernel's instruction footprint matters.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
-        if (mbar_try_wait_hint(bar, parity, 1000u)) return true;
+                                          uint32_t max_polls = 1u << 17) {
+#pragma unroll 1
+    for (uint32_t i = 0; i < max_polls; ++i) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
         if (abort && *abort) return false;
-        if (i >= 4) __nanosleep(32);
-        if ((i & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) break;
     }
     if (abort) *abort = 1;
     return false;
+}
+
+// ------------------------------------------------------ register rebalancing
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+// The increases draw on what the decreases released: the sum over the
+// warpgroups never exceeds the block's launch allocation.
+template <int N> __device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N> __device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------- fences
@@ -120,6 +130,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+// Prefetch of a 3-D tile into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
 }
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
                                             int y) {
@@ -213,8 +229,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -251,11 +282,44 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-// 2^x on the special-function unit (PTX ex2.approx.f32, relative error
-// about 2^-22 over the range used here: x <= 0).
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32, relative error
+// about 2^-22; results below 2^-126 flush to zero, which for the decay
+// factors here (all <= 1) drops terms under 1e-38 of the largest ones).
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------- warp-level tensor-core MMA
+// Used for the small 16x16 block products of the triangular solve, where a
+// single warp owns the whole dependency chain (latency, not throughput).
+//
+// ldmatrix: four 8x8 b16 matrices; lane l supplies the address of row (l % 8)
+// of matrix (l / 8). Thread t receives, of matrix m, the pair at row t / 4,
+// columns 2 (t % 4) .. + 1 (or, with .trans, the transposed pair).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// D = A B + D, m16n8k16, fp16 A (row) and B (col), fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// log2 on the special-function unit; lg2(+0) = -inf (so exp2 of it is 0).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
