@@ -68,13 +68,13 @@ struct TcArgs {
 namespace tck {
 constexpr int C = 64, D = 128;
 constexpr int KQ_STAGES = 3, V_STAGES = 2, GB_SLOTS = 3;
-constexpr int NTHREADS = 640;
-// Registers: launched with REGS_LAUNCH per thread (640 x 96 = 61440). The
-// single-thread roles and the prep groups give some up; the two state
+constexpr int NTHREADS = 512;
+// Registers: launched with REGS_LAUNCH per thread (512 x 128 = 65536). The
+// single-thread roles give some up; the prep warps and the two state
 // warpgroups (64 fp32 state values per thread) take them:
-// 128 x (48 + 80 + 80 + 136 + 136) = 61440.
-constexpr int REGS_LAUNCH = 96, REGS_ROLES = 48, REGS_PREP = 80, REGS_STATE = 136;
-static_assert(128 * (REGS_ROLES + 2 * REGS_PREP + 2 * REGS_STATE) <= NTHREADS * REGS_LAUNCH,
+// 128 x (48 + 160 + 152 + 152) = 65536.
+constexpr int REGS_LAUNCH = 128, REGS_ROLES = 48, REGS_PREP = 160, REGS_STATE = 152;
+static_assert(128 * (REGS_ROLES + REGS_PREP + 2 * REGS_STATE) <= NTHREADS * REGS_LAUNCH,
               "register rebalancing exceeds the launch allocation");
 // TMEM columns
 constexpr uint32_t T_SACC = 0, T_DU = 128, T_O = 192, T_X = 256, T_W = 320, T_ST = 384, T_DT = 448,
@@ -89,12 +89,12 @@ constexpr uint32_t OFF_WT = OFF_V + V_STAGES * V_BYTES;  // -W^T, MN-major B: 12
 constexpr uint32_t OFF_BW = OFF_WT + 16384;              // Bw x 2 buffers, K-major B: 64 rows (r) x 128 B (s)
 constexpr uint32_t OFF_BU = OFF_BW + 16384;              // Bu x 2 buffers
 constexpr uint32_t OFF_P = OFF_BU + 16384;               // P x 2 buffers, K-major B
-// per prep group (x 2): A fp16 (64 rows x 128 B, 128-byte swizzle), the
-// diagonal 16x16 blocks of A in fp32 (column-major), those of T in fp16
+// prep: A fp16 (64 rows x 128 B, 128-byte swizzle), the diagonal 16x16
+// blocks of A in fp32 (column-major), those of T in fp16
 constexpr uint32_t OFF_AS = OFF_P + 16384;
-constexpr uint32_t OFF_AD = OFF_AS + 2 * 8192;
-constexpr uint32_t OFF_TS = OFF_AD + 2 * 4096;
-constexpr uint32_t OFF_GB = OFF_TS + 2 * 2048;
+constexpr uint32_t OFF_AD = OFF_AS + 8192;
+constexpr uint32_t OFF_TS = OFF_AD + 4096;
+constexpr uint32_t OFF_GB = OFF_TS + 2048;
 constexpr uint32_t GB_FLOATS = 6 * 64 + 4;               // G, gam, bet, bg, dec, qsc, gC
 constexpr uint32_t GB_SLOT_BYTES = GB_FLOATS * 4;
 constexpr uint32_t OFF_BAR = OFF_GB + GB_SLOTS * GB_SLOT_BYTES;
@@ -109,10 +109,10 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 // barrier indices
 enum {
     B_FULL_KQ = 0, B_EMPTY_KQ = 3, B_FULL_V = 6, B_EMPTY_V = 8, B_GB_FULL = 10, B_GB_EMPTY = 13,
-    B_XREADY0 = 16, B_XREADY1, B_XFREE, B_BWU0, B_BWU1, B_M2DONE0, B_M2DONE1, B_WREADY, B_DREADY, B_DELTA,
-    B_SREADY, B_STREADY, B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE, B_CONV0, B_CONV1
+    B_XREADY0 = 16, B_XREADY1, B_XFREE, B_BWU0, B_BWU1, B_M2W0, B_M2W1, B_WREADY, B_DREADY, B_DELTA,
+    B_SREADY, B_STREADY, B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE, B_CONV0, B_CONV1, B_M2U0, B_M2U1
 };
-static_assert(B_CONV1 < (int)NUM_BARS, "barrier count");
+static_assert(B_M2U1 < (int)NUM_BARS, "barrier count");
 
 // gb slot fields (float offsets)
 constexpr int GB_G = 0, GB_GAM = 64, GB_BET = 128, GB_BG = 192, GB_DEC = 256, GB_QSC = 320, GB_GC = 384;
@@ -273,7 +273,7 @@ __device__ __forceinline__ void solve_block_row(int bi, uint32_t as_u, uint32_t 
     }
 }
 
-// A/P pass of one prep group on chunk n (its A and Ad tiles and P buffer
+// A/P pass of the prep warps on chunk n (the A and Ad tiles and P buffer
 // n & 1): from X = [K; Q] K^T in TMEM, row r of A (rows 0-63, TMEM lanes
 // 0-63) or of P (lanes 64-127) per thread; gt = the thread's TMEM lane.
 __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float* gb, int n, int len, float scale,
@@ -282,8 +282,8 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
     const int wq = gt >> 5;
     const int grp = n & 1;
     const uint32_t lane_base = (uint32_t)(32 * wq) << 16;
-    uint8_t* As = sm + OFF_AS + (uint32_t)grp * 8192;
-    float* Ad = reinterpret_cast<float*>(sm + OFF_AD + (uint32_t)grp * 4096);
+    uint8_t* As = sm + OFF_AS;
+    float* Ad = reinterpret_cast<float*>(sm + OFF_AD);
     // ---- A = strictly-lower(diag(beta) Gamma o K K^T) (fp16 tile + fp32
     //      diagonal blocks) and P = scale (Gamma o Q K^T) masked r >= s
     //      (fp16 B tile). Rows 0-31 only have columns 0-31.
@@ -294,44 +294,46 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
         const float base = gb[GB_G + r] + (isA ? lg2(gb[GB_BET + r]) : lg2(scale));
         // kept columns: s < r (A), s <= r on live rows (P)
         const int lim = isA ? r : (r < min(C, len - n * C) ? r + 1 : 0);
-        const float4* G4 = reinterpret_cast<const float4*>(gb + GB_G);
         uint8_t* row = isA ? As + r * 128 : sm + OFF_P + (uint32_t)grp * 8192 + r * 128;
         const bool wide = (wq & 1) != 0;  // rows 32-63
 #pragma unroll 1
-        for (int hc = 0; hc < 2; ++hc) {  // halves of 32 columns, one TMEM load each
-            if (hc == 1 && !wide) break;
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_base + T_X + 32 * hc, x);
+        for (int qc = 0; qc < 4; ++qc) {  // quarters of 16 columns (rows 0-31 need only 0-31)
+            if (qc >= 2 && !wide) break;
+            uint32_t x[16];
+            if (qc == 0 && gt == 0) GDN_TRACE_AT(7, n);
+            tmem_ld16(tmem + lane_base + T_X + 16 * qc, x);
             tmem_ld_wait();
-            // in place: x[e] becomes the fp32 value of column 32 hc + e
-            const float4* src = G4 + 8 * hc;
+            if (qc == 0 && gt == 0) GDN_TRACE_AT(8, n);
+            // in place: x[e] becomes the fp32 value of column 16 qc + e
+            const uint32_t src = smem_u32(gb + GB_G) + 64u * (uint32_t)qc;
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 g4 = src[q4];
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 g4 = lds_f4(src + 16u * (uint32_t)q4);
                 const float gq[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
                 for (int e4 = 0; e4 < 4; ++e4) {
                     const int e = 4 * q4 + e4;
                     // Gamma_rs = exp(G_r - G_s) <= 1 for s <= r (beta_r / scale folded in)
-                    x[e] = __float_as_uint((32 * hc + e < lim) ? ex2(base - gq[e4]) * __uint_as_float(x[e]) : 0.f);
+                    x[e] = __float_as_uint((16 * qc + e < lim) ? ex2(base - gq[e4]) * __uint_as_float(x[e]) : 0.f);
                 }
             }
+            if (qc == 0 && gt == 0) GDN_TRACE_AT(9, n);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                const int c = 4 * hc + c4;
+            for (int c2 = 0; c2 < 2; ++c2) {
+                const int c = 2 * qc + c2;
                 uint4 u;
-                u.x = h2(__uint_as_float(x[8 * c4 + 0]), __uint_as_float(x[8 * c4 + 1]));
-                u.y = h2(__uint_as_float(x[8 * c4 + 2]), __uint_as_float(x[8 * c4 + 3]));
-                u.z = h2(__uint_as_float(x[8 * c4 + 4]), __uint_as_float(x[8 * c4 + 5]));
-                u.w = h2(__uint_as_float(x[8 * c4 + 6]), __uint_as_float(x[8 * c4 + 7]));
+                u.x = h2(__uint_as_float(x[8 * c2 + 0]), __uint_as_float(x[8 * c2 + 1]));
+                u.y = h2(__uint_as_float(x[8 * c2 + 2]), __uint_as_float(x[8 * c2 + 3]));
+                u.z = h2(__uint_as_float(x[8 * c2 + 4]), __uint_as_float(x[8 * c2 + 5]));
+                u.w = h2(__uint_as_float(x[8 * c2 + 6]), __uint_as_float(x[8 * c2 + 7]));
                 *reinterpret_cast<uint4*>(row + ((((uint32_t)c ^ (uint32_t)r) & 7u) << 4)) = u;
             }
-            if (isA && ((r >> 5) == hc)) {  // diagonal 16x16 block in fp32, column-major
-                const int h16 = (r >> 4) & 1;
+            if (isA && ((r >> 4) == qc)) {  // diagonal 16x16 block in fp32, column-major
                 float* dcol = Ad + (r >> 4) * 256 + (r & 15);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dcol[16 * e] = __uint_as_float(h16 ? x[16 + e] : x[e]);
+                for (int e = 0; e < 16; ++e) dcol[16 * e] = __uint_as_float(x[e]);
             }
+            if (qc == 0 && gt == 0) GDN_TRACE_AT(6, n);
         }
         if (!isA) fence_async_smem();
     }
@@ -376,7 +378,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         for (int i = 0; i < GB_SLOTS; ++i) { mbar_init(&bars[B_GB_FULL + i], 1); mbar_init(&bars[B_GB_EMPTY + i], 12); }
         mbar_init(&bars[B_XREADY0], 1); mbar_init(&bars[B_XREADY1], 1); mbar_init(&bars[B_XFREE], 4);
         mbar_init(&bars[B_BWU0], 4); mbar_init(&bars[B_BWU1], 4);
-        mbar_init(&bars[B_M2DONE0], 1); mbar_init(&bars[B_M2DONE1], 1); mbar_init(&bars[B_WREADY], 4);
+        mbar_init(&bars[B_M2W0], 1); mbar_init(&bars[B_M2W1], 1); mbar_init(&bars[B_WREADY], 8);
+        mbar_init(&bars[B_M2U0], 1); mbar_init(&bars[B_M2U1], 1);
         mbar_init(&bars[B_DREADY], 1); mbar_init(&bars[B_DELTA], 8); mbar_init(&bars[B_SREADY], 1);
         mbar_init(&bars[B_STREADY], 8); mbar_init(&bars[B_OREADY], 1); mbar_init(&bars[B_OFREE], 8);
         mbar_init(&bars[B_PFREE0], 1); mbar_init(&bars[B_PFREE1], 1); mbar_init(&bars[B_DONE], 2);
@@ -405,16 +408,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     // warp-uniform wait (every lane polls; the warp proceeds only if all saw it)
     auto WAITW = [&](int b, uint32_t parity) { return __all_sync(0xffffffffu, WAIT(b, parity)) != 0; };
 
-    // Roles (20 warps). Each role's register budget is set at the top of its
+    // Roles (16 warps). Each role's register budget is set at the top of its
     // own branch, so that the compiler allocates that role's code within it.
     //   warp 0        TMA producer (K, Q, V tiles; L2 prefetch 3 chunks ahead)
-    //   warp 1        state-dependent products M3a, M3b, M5, M4; owns TMEM
-    //   warp 2        look-ahead products M1, M2
+    //   warp 1        chunk-order products M2u, M3a, M3b, M5, M4; owns TMEM
+    //   warp 2        look-ahead products M1, M2w
     //   warp 3        g, beta -> cumulative decay and factors per chunk
-    //   warps 4-7     prep group 0 (even chunks), warps 8-11 group 1 (odd):
-    //                 A/P, triangular solve, -W^T hand-off
-    //   warps 12-19   state: thread (j, half) holds half of column j of S (fp32);
-    //                 between chunks, the bf16 -> fp16 operands two chunks ahead
+    //   warps 4-7     prep: A/P and the triangular solve (Bw, Bu)
+    //   warps 8-15    state: thread (j, half) holds half of column j of S (fp32);
+    //                 the -W^T hand-off one chunk ahead while M5 runs, and the
+    //                 bf16 -> fp16 operands two chunks ahead between chunks
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         regs_dec<REGS_ROLES>();
@@ -460,12 +463,29 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const uint32_t id_n64_mn = idesc_f16(128, 64, false, true);
             const uint32_t id_n64_k = idesc_f16(128, 64, false, false);
             const uint32_t id_n128_mn = idesc_f16(128, 128, false, true);
+            const uint32_t id_wu = idesc_f16(128, 64, true, false);
             const uint32_t wt = smem_u32(sm + OFF_WT);
             for (int n = 0; n < nc; ++n) {
+                // M2u: U^T = V^T Bu^T into the Delta accumulator. Issued here, in
+                // program order after M5(n-1) (so Delta(n-1) has been read out)
+                // and before M3a(n), which accumulates onto it; needs T of chunk
+                // n (BWU) and the fp16 V (CONV).
+                if (!WAIT(B_CONV0 + (n & 1), (n >> 1) & 1) || !WAIT(B_BWU0 + (n & 1), (n >> 1) & 1)) break;
+                tc_fence_after();
+                {
+                    const uint32_t vt = smem_u32(v_tile(n));
+                    const uint32_t bu = smem_u32(sm + OFF_BU + (uint32_t)(n & 1) * 8192);
+#pragma unroll 1
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + T_DU, sdesc_sw128(vt + kk * 2048, 8192, 1024),
+                                 sdesc_sw128(bu + kk * 32, 16, 1024), id_wu, kk > 0 ? 1u : 0u);
+                    mma_commit(&bars[B_M2U0 + (n & 1)]);
+                    mma_commit(&bars[B_EMPTY_V + n % V_STAGES]);
+                }
                 if (!WAIT(B_WREADY, n & 1) || !WAIT(B_STREADY, n & 1)) break;
                 GDN_TRACE_AT(20, n);
                 tc_fence_after();
-                // M3a: D^T = U^T + S^T (-W)^T  (accumulates onto U^T written by M2)
+                // M3a: D^T = U^T + S^T (-W)^T  (accumulates onto U^T written by M2u)
 #pragma unroll 1
                 for (int kk = 0; kk < 8; ++kk)
                     mma_bf16_ts(tmem + T_DU, tmem + T_ST + 8 * kk, sdesc_sw128(wt + kk * 2048, 16384, 1024), id_n64_mn, 1u);
@@ -501,13 +521,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         }
     } else if (warp == 2) {
         // ------------------------------------------------- look-ahead products
-        // Issue order M1(0), then per chunk m: M1(m+1), M2(m). M1(m+1) needs the
-        // stage and X released by the prep group of m (A/P done); M2(m) needs
-        // the prep group of m done (T: BWU), chunk m converted (fp16 K, V:
-        // CONV) and the U and W regions released by chunk m-1. The state warps
-        // wait for M1(c) before converting chunk c; the next phase of that
-        // XREADY barrier is M1(c+2), which this order issues after M2(c), i.e.
-        // after conversion c was seen.
+        // Issue order M1(0), then per chunk m: M1(m+1), M2w(m). M1(m+1) needs the
+        // stage and X released by the prep group of m (A/P done); M2w(m) (-W^T,
+        // the W half of M2) needs the prep group of m done (T: BWU), chunk m
+        // converted (fp16 K: CONV) and the W region read out for chunk m-1.
+        // The state warps wait for M1(c) before converting chunk c; the next
+        // phase of that XREADY barrier is M1(c+2), which this order issues after
+        // M2w(c), i.e. after conversion c was seen.
         regs_dec<REGS_ROLES>();
         if (lane == 0) {
             const uint32_t id_x = idesc_bf16(128, 64, false, false);  // raw bf16 K, Q
@@ -522,20 +542,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 }
                 mma_commit(&bars[B_XREADY0 + (n & 1)]);
             };
-            auto issue_m2 = [&](int n) {
-                const uint32_t kq = smem_u32(kq_tile(n)), vt = smem_u32(v_tile(n));
+            auto issue_m2w = [&](int n) {
+                const uint32_t kq = smem_u32(kq_tile(n));
                 const uint32_t bw = smem_u32(sm + OFF_BW + (uint32_t)(n & 1) * 8192);
-                const uint32_t bu = smem_u32(sm + OFF_BU + (uint32_t)(n & 1) * 8192);
 #pragma unroll 1
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + T_W, sdesc_sw128(kq + kk * 2048, 16384, 1024), sdesc_sw128(bw + kk * 32, 16, 1024),
                              id_wu, kk > 0 ? 1u : 0u);
-#pragma unroll 1
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + T_DU, sdesc_sw128(vt + kk * 2048, 8192, 1024), sdesc_sw128(bu + kk * 32, 16, 1024),
-                             id_wu, kk > 0 ? 1u : 0u);
-                mma_commit(&bars[B_M2DONE0 + (n & 1)]);
-                mma_commit(&bars[B_EMPTY_V + n % V_STAGES]);
+                mma_commit(&bars[B_M2W0 + (n & 1)]);
             };
             if (nc > 0 && WAIT(B_FULL_KQ, 0)) {
                 tc_fence_after();
@@ -551,10 +565,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                         issue_m1(m + 1);
                     }
                     if (!WAIT(B_CONV0 + (m & 1), (m >> 1) & 1) || !WAIT(B_BWU0 + (m & 1), (m >> 1) & 1)) break;
-                    if (m >= 1 && (!WAIT(B_DELTA, (m - 1) & 1) || !WAIT(B_WREADY, (m - 1) & 1))) break;
+                    if (m >= 1 && !WAIT(B_WREADY, (m - 1) & 1)) break;
                     tc_fence_after();
                     GDN_TRACE_AT(31, m);
-                    issue_m2(m);
+                    issue_m2w(m);
                 }
             }
             mma_commit(&bars[B_DONE]);
@@ -598,27 +612,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (lane == 0) mbar_arrive(&bars[B_GB_FULL + slot]);
             if (lane == 0) GDN_TRACE_AT(41, n);
         }
-    } else if (warp < 12) {
-        // ---------------------------------------------------------- prep groups
-        // group g = 0 (warps 4-7) takes the even chunks, g = 1 (warps 8-11) the
-        // odd ones; each owns the A, Ad, Ts tiles, Bw/Bu and P buffers g
-        regs_dec<REGS_PREP>();
-        const int g = (warp - 4) >> 2;
-        const int gt = threadIdx.x - 128 - 128 * g;  // 0..127 = TMEM lane
+    } else if (warp < 8) {
+        // ----------------------------------------------------------------- prep
+        // all chunks in order; the Bw/Bu and P buffers and the per-parity
+        // barriers of chunk n are those of index g = n & 1
+        regs_inc<REGS_PREP>();
+        const int gt = threadIdx.x - 128;  // 0..127 = TMEM lane
         const int wq = gt >> 5;
-        const int bar_id = 1 + g;
-        uint8_t* As = sm + OFF_AS + (uint32_t)g * 8192;
-        float* Ad = reinterpret_cast<float*>(sm + OFF_AD + (uint32_t)g * 4096);
-        uint8_t* Ts = sm + OFF_TS + (uint32_t)g * 2048;
-        uint8_t* bw = sm + OFF_BW + (uint32_t)g * 8192;
-        uint8_t* bu = sm + OFF_BU + (uint32_t)g * 8192;
-        for (int n = g; n < nc; n += 2) {
+        const int bar_id = 1;
+        uint8_t* As = sm + OFF_AS;
+        float* Ad = reinterpret_cast<float*>(sm + OFF_AD);
+        uint8_t* Ts = sm + OFF_TS;
+        for (int n = 0; n < nc; ++n) {
+            const int g = n & 1;
+            uint8_t* bw = sm + OFF_BW + (uint32_t)g * 8192;
+            uint8_t* bu = sm + OFF_BU + (uint32_t)g * 8192;
             const float* gb = gb_slot(n);
-            const uint32_t ph = (uint32_t)(n >> 1) & 1u;  // phase parity of this group's barriers
+            const uint32_t ph = (uint32_t)(n >> 1) & 1u;  // phase parity of the per-parity barriers
             bool ok = WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1) && WAITW(B_XREADY0 + g, ph);
             // P and Bw/Bu buffers g were last read by the products of chunk n - 2
             if (ok && wq >= 2 && n >= 2) ok = WAITW(B_PFREE0 + g, ph ^ 1u);
-            if (ok && n >= 2) ok = WAITW(B_M2DONE0 + g, ph ^ 1u);
+            if (ok && n >= 2) ok = WAITW(B_M2W0 + g, ph ^ 1u) && WAITW(B_M2U0 + g, ph ^ 1u);
             if (named_sync_or(bar_id, 128, !ok)) break;
             if (gt == 0) GDN_TRACE_AT(0, n);
             tc_fence_after();
@@ -674,35 +688,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 mbar_arrive(&bars[B_GB_EMPTY + n % GB_SLOTS]);
             }
             if (gt == 0) GDN_TRACE_AT(4, n);
-            // ---- -W^T of chunk n from TMEM (lane = key index i = gt, columns =
-            //      chunk rows r) into the MN-major fp16 B tile of M3a, once M2(n)
-            //      has run and M3a(n-1) has finished reading the tile
-            ok = WAITW(B_M2DONE0 + g, ph) && (n < 1 || WAITW(B_DREADY, (n - 1) & 1));
-            if (named_sync_or(bar_id, 128, !ok)) break;
-            tc_fence_after();
-            {
-                const uint32_t lb = (uint32_t)(32 * wq) << 16;
-#pragma unroll
-                for (int hq = 0; hq < 2; ++hq) {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lb + T_W + 32 * hq, w);
-                    tmem_ld_wait();
-                    store_half_row_sw128(sm + OFF_WT, (uint32_t)gt, reinterpret_cast<const float*>(w), hq);
-                }
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_WREADY]);
-            if (gt == 0) GDN_TRACE_AT(13, n);
         }
     } else {
         // ---------------------------------------------------------------- state
-        // warps 12-19: thread (j, hf) holds rows 64 hf .. 64 hf + 63 of column j
+        // warps 8-15: thread (j, hf) holds rows 64 hf .. 64 hf + 63 of column j
         // of S in fp32 for the whole sequence; handles chunk rows 32 hf .. + 31
         // of Delta^T and of the output
         regs_inc<REGS_STATE>();
-        const int ws = warp - 12, q4 = warp & 3, hf = ws >> 2;
+        const int ws = warp - 8, q4 = warp & 3, hf = ws >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const size_t sbase = ((size_t)n_seq * p.h_v + h) * (size_t)(D * D);
@@ -791,6 +784,28 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_DELTA]);
+            }
+            // -W^T of chunk n + 1 from TMEM (lane = key index i = j, columns =
+            // chunk rows r; this thread: rows 32 hf .. + 31) into the MN-major
+            // fp16 B tile of M3a, once M2w(n + 1) has run; M3a(n) has finished
+            // reading the tile (DREADY(n) was seen). Runs while M5(n) does.
+            if (n + 1 >= 0 && n + 1 < nc) {
+                if (!WAITW(B_M2W0 + ((n + 1) & 1), ((n + 1) >> 1) & 1)) break;
+                tc_fence_after();
+                {
+                    uint32_t w[32];
+                    tmem_ld32(tmem + lane_base + T_W + 32 * hf, w);
+                    tmem_ld_wait();
+                    store_half_row_sw128(sm + OFF_WT, (uint32_t)j, reinterpret_cast<const float*>(w), hf);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[B_WREADY]);
+                if (ws == 0 && lane == 0) GDN_TRACE_AT(13, n + 1);
+            }
+            if (n >= 0) {
+                const float* gb = gb_slot(n);
                 // state update S^T <- gamma_last S^T + Delta^T Kdec
                 const float gC = gb[GB_GC];
                 if (!WAITW(B_SREADY, n & 1)) break;
@@ -816,9 +831,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!WAITW(B_OREADY, n & 1)) break;
                 tc_fence_after();
                 {
-                    // o[t0 + n C + r][h][j] for r < nv: one row per register; a byte
-                    // pointer stepped by the token stride (the full-chunk case has no
-                    // per-row test)
+                    // o[t0 + n C + r][h][j] for r < nv: one row per register, through a
+                    // byte pointer stepped by the token stride
                     const int nv = min(C, len - n * C) - 32 * hf;  // valid rows of this half
                     char* orow = reinterpret_cast<char*>(o + ((size_t)(t0 + (long long)n * C + 32 * hf) * p.h_v + h) * D + j);
                     const size_t ostep = (size_t)p.h_v * D * sizeof(TOut);

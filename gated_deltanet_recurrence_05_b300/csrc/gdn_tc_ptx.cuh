@@ -95,6 +95,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// ------------------------------------------------------ shared-memory access
+// Explicit shared-space loads and stores (32-bit shared addresses), for the
+// hot paths: they are tracked on the short scoreboard like any LDS/STS.
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr));
+    return v;
+}
+
 // ------------------------------------------------------ register rebalancing
 // Per-warpgroup register budget (all four warps of a warpgroup execute it).
 // The increases draw on what the decreases released: the sum over the
