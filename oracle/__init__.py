@@ -10,6 +10,8 @@ numpy / torch CPU arrays into it and back.
 
   recurrent(...)  token-by-token gated delta rule (the oracle proper)
   chunked(...)    the chunkwise algebra, used only to pin that algebra
+  gated_rmsnorm(...)  the output epilogue (zero-centred RMSNorm times a
+                  sigmoid gate), numpy fp64, in ``epilogue.py``
 
 Both return ``(o, S)``: with ``pairs=None`` o is [T_total, H_v, d_v] and S is
 [N, H_v, d_k, d_v] (float64 numpy); with ``pairs=[(n, h), ...]`` they are
@@ -27,6 +29,8 @@ import subprocess
 import threading
 
 import numpy as np
+
+from .epilogue import gated_rmsnorm, rms_normalize, sigmoid  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
