@@ -307,6 +307,7 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
+    epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -323,7 +324,7 @@ def run_ours(args, world, rank, local):
                    "global_batch": N * world, "seq_len": T // N, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (126 MB) every step; no flush"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
-        "clocks": clk.summary(), "decode": decode,
+        "clocks": clk.summary(), "decode": decode, "epilogue": epilogue,
     }
 
 
@@ -369,6 +370,71 @@ def run_decode(args, dev, peaks, world):
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
 
 
+def run_epilogue(args, dev, peaks, world, o):
+    """The GDN output epilogue (zero-centred RMSNorm x sigmoid gate): standalone
+    on the prefill output, and fused into the decode step."""
+    import gated_deltanet_recurrence_05_b300 as gdn
+    gen = torch.Generator().manual_seed(args.seed + 99)
+    z = torch.randn(o.shape, generator=gen).to(torch.bfloat16).to(dev)
+    wn = (torch.randn(o.shape[-1], generator=gen) * 0.2).to(dev)
+    y = torch.empty_like(o)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, args.steps)
+    for _ in range(3):
+        gdn.gated_rmsnorm(o, z, wn, out=y, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(reps):
+        gdn.gated_rmsnorm(o, z, wn, out=y, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+    b = 3 * o.numel() * o.element_size() + wn.numel() * 4
+    gbs = b / (us / 1e6) / 1e9
+    out = {"standalone": {"workload": f"gated RMSNorm on the prefill output {list(o.shape)} bf16 (gate bf16, "
+                                      f"weight fp32), > L2 every launch",
+                          "us_per_launch": us, "GB_per_s": gbs * world, "gpu_launches": reps,
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                       "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                       "algorithmic_bytes_per_launch": int(b)}}}
+    if not args.skip_decode:
+        wl = gdn_inputs.WORKLOADS["decode"]
+        steps = min(args.decode_steps, 200)
+        d = gdn_inputs.make_workload("decode", steps=steps, seed=args.seed)
+        dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+        state = dd["state"].clone()
+        od = torch.empty(wl.num_seqs, wl.h_v, wl.d_v, dtype=torch.bfloat16, device=dev)
+        zd = torch.randn(steps, wl.num_seqs, wl.h_v, wl.d_v, generator=gen).to(torch.bfloat16).to(dev)
+        wd = (torch.randn(wl.d_v, generator=gen) * 0.2).to(dev)
+
+        def run(n0, n1):
+            for t in range(n0, n1):
+                gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state, out=od,
+                                gate=zd[t], norm_weight=wd, stream=stream)
+
+        run(0, min(3, steps))
+        torch.cuda.synchronize(dev)
+        state.copy_(dd["state"])
+        barrier(world)
+        ev0.record(stream)
+        run(0, steps)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if gdn.get_device_error() != 0:
+            raise RuntimeError("device error in the gated decode")
+        us_d = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / steps, world, dev)
+        bd = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v) + zd[0].numel() * 2 + wd.numel() * 4
+        gbd = bd / (us_d / 1e6) / 1e9
+        out["fused_decode"] = {"workload": "the decode workload with the epilogue fused (gate bf16 per step)",
+                               "us_per_step": us_d, "gpu_launches": steps,
+                               "roofline": {"bound": "hbm", "achieved": round(gbd, 1), "peak": peaks["hbm_gbs"],
+                                            "unit": "GB/s", "frac": round(gbd / peaks["hbm_gbs"], 4),
+                                            "algorithmic_bytes_per_launch": int(bd)}}
+    return out
+
+
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores (bounded sample)."""
     if rank != 0:
@@ -407,6 +473,7 @@ def main(argv=None):
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the prefill kernel from an ncu capture")
     ap.add_argument("--skip-decode", action="store_true")
+    ap.add_argument("--skip-epilogue", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -56,6 +56,11 @@ def lib():
         L.gdn_chunk_fwd.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, F, P]
         L.gdn_decode_step.restype = ctypes.c_int
+        L.gdn_decode_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, F, I32, I32, I32, I32, I32, I32,
+                                            I32, F, P]
+        L.gdn_decode_step_gated.restype = ctypes.c_int
+        L.gdn_gated_rmsnorm.argtypes = [P, P, P, P, I64, I32, I32, I32, F, P]
+        L.gdn_gated_rmsnorm.restype = ctypes.c_int
         L.gdn_plan_seq_order.argtypes = [P, I32, P]
         L.gdn_plan_seq_order.restype = ctypes.c_int
         L.gdn_get_device_error.argtypes = [P, P]
@@ -144,10 +149,14 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                 beta: torch.Tensor, state: torch.Tensor, *, output_dtype: Optional[torch.dtype] = None,
-                scale: float = 0.0, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                scale: float = 0.0, out: Optional[torch.Tensor] = None, gate: Optional[torch.Tensor] = None,
+                norm_weight: Optional[torch.Tensor] = None, eps: float = 1e-6, stream=None) -> torch.Tensor:
     """One token for N sequences; ``state`` [N, H_v, d_k, d_v] is updated in place.
 
     q, k: [N, H_qk, d_k]; v: [N, H_v, d_v]; g, beta: [N, H_v] fp32. Returns o [N, H_v, d_v].
+    With ``gate`` ([N, H_v, d_v], dtype of q) the output goes through the gated
+    RMSNorm epilogue (``gated_rmsnorm``), fused into the decode kernel for
+    d_k = d_v = 128; ``norm_weight`` [d_v] fp32 is its zero-centred weight.
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
         _dev(t, name)
@@ -155,11 +164,47 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     h_v, d_v = v.shape[1], v.shape[2]
     odt = output_dtype or v.dtype
     o = out if out is not None else torch.empty((N, h_v, d_v), dtype=odt, device=v.device)
-    st = lib().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o),
-                               N, h_qk, h_v, d_k, d_v, _code(q), _code(o), float(scale),
-                               _stream(stream))
-    _check("gdn_decode_step", st)
+    if gate is None:
+        if norm_weight is not None:
+            raise ValueError("norm_weight needs a gate")
+        st = lib().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o),
+                                   N, h_qk, h_v, d_k, d_v, _code(q), _code(o), float(scale),
+                                   _stream(stream))
+        _check("gdn_decode_step", st)
+        return o
+    _dev(gate, "gate")
+    if gate.dtype != q.dtype or tuple(gate.shape) != (N, h_v, d_v):
+        raise ValueError("gate must be [N, H_v, d_v] in the dtype of q")
+    if norm_weight is not None:
+        _dev(norm_weight, "norm_weight")
+    st = lib().gdn_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o),
+                                     _ptr(gate), _ptr(norm_weight), float(eps), N, h_qk, h_v, d_k, d_v,
+                                     _code(q), _code(o), float(scale), _stream(stream))
+    _check("gdn_decode_step_gated", st)
     return o
+
+
+def gated_rmsnorm(x: torch.Tensor, gate: torch.Tensor, norm_weight: Optional[torch.Tensor] = None, *,
+                  eps: float = 1e-6, out: Optional[torch.Tensor] = None,
+                  output_dtype: Optional[torch.dtype] = None, stream=None) -> torch.Tensor:
+    """GDN output epilogue over the last axis: x / rms(x) * (1 + norm_weight) * sigmoid(gate).
+
+    x, gate: [..., d] (same shape and dtype; e.g. the prefill output [T, H_v, d_v]);
+    norm_weight: [d] fp32 or None. ``out`` may be ``x`` itself (in place).
+    """
+    _dev(x, "x")
+    _dev(gate, "gate")
+    if gate.dtype != x.dtype or gate.shape != x.shape:
+        raise ValueError("gate must match x in shape and dtype")
+    if norm_weight is not None:
+        _dev(norm_weight, "norm_weight")
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    y = out if out is not None else torch.empty(x.shape, dtype=output_dtype or x.dtype, device=x.device)
+    st = lib().gdn_gated_rmsnorm(_ptr(x), _ptr(gate), _ptr(norm_weight), _ptr(y), rows, d, _code(x), _code(y),
+                                 float(eps), _stream(stream))
+    _check("gdn_gated_rmsnorm", st)
+    return y
 
 
 def plan_seq_order(cu_seqlens) -> torch.Tensor:

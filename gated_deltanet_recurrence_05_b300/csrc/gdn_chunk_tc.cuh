@@ -38,14 +38,14 @@
 // below the fp16 range contribute less than 1e-7 of the largest terms. The
 // path therefore assumes |v| and |S| stay well below 6e4 (the fp16 range).
 //
-// Warp roles (640 threads) are listed where they branch (chunk_tc_kernel).
-// Two prep groups work on alternate chunks so that the per-chunk solve, whose
-// steps are short and dependent, overlaps; the state warps convert operands
-// two chunks ahead in the time they would otherwise wait. The instruction
-// footprint is kept small on purpose (rolled issue loops, one copy of each
-// step): with 20 warps running different code the instruction cache was the
-// first bottleneck. All waits are bounded (a timeout raises an abort flag,
-// records GDN_DEVERR_TIMEOUT and every role unwinds); TMEM is always freed.
+// Warp roles (512 threads) are listed where they branch (chunk_tc_kernel).
+// One group of four prep warps builds T for every chunk (A/P pass, then the
+// blocked solve); the state warps convert operands two chunks ahead in the
+// time they would otherwise wait. The instruction footprint is kept small on
+// purpose (rolled issue and conversion loops, one copy of each step): with 16
+// warps running different code the instruction cache was the first
+// bottleneck. All waits are bounded (a timeout raises an abort flag, records
+// GDN_DEVERR_TIMEOUT and every role unwinds); TMEM is always freed.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -119,33 +119,11 @@ constexpr int GB_G = 0, GB_GAM = 64, GB_BET = 128, GB_BG = 192, GB_DEC = 256, GB
 
 __device__ __forceinline__ uint32_t h2(float lo, float hi) { return tc::pack_f16x2(lo, hi); }
 __device__ __forceinline__ float2 unbf2(uint32_t u) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
-    return __bfloat1622float2(v);
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 __device__ __forceinline__ float2 unh2(uint32_t u) {
     __half2 v = *reinterpret_cast<__half2*>(&u);
     return __half22float2(v);
-}
-// One 128-byte tile row (64 values): bf16 in, fp16 out (times f when
-// SCALED), in place. All eight 16-byte loads are issued before any store:
-// the swizzled indices are runtime values, so the compiler could not
-// otherwise move a load above the previous chunk's store.
-template <bool SCALED>
-__device__ __forceinline__ void bf16_row_to_f16(uint8_t* row, uint32_t r, float f) {
-    uint4* p = reinterpret_cast<uint4*>(row);
-    uint4 u[8];
-#pragma unroll
-    for (int c0 = 0; c0 < 8; ++c0) u[c0] = p[((uint32_t)c0 ^ r) & 7u];
-#pragma unroll
-    for (int c0 = 0; c0 < 8; ++c0) {
-        float2 a = unbf2(u[c0].x), b = unbf2(u[c0].y), d = unbf2(u[c0].z), e = unbf2(u[c0].w);
-        if (SCALED) {
-            a.x *= f; a.y *= f; b.x *= f; b.y *= f; d.x *= f; d.y *= f; e.x *= f; e.y *= f;
-        }
-        u[c0].x = h2(a.x, a.y); u[c0].y = h2(b.x, b.y); u[c0].z = h2(d.x, d.y); u[c0].w = h2(e.x, e.y);
-    }
-#pragma unroll
-    for (int c0 = 0; c0 < 8; ++c0) p[((uint32_t)c0 ^ r) & 7u] = u[c0];
 }
 // Write 64 floats v[0..63] as fp16 into row `row` of a 128B-swizzled tile.
 __device__ __forceinline__ void store_row_sw128(uint8_t* tile, uint32_t row, const float* v) {
@@ -177,7 +155,7 @@ __device__ __forceinline__ void store_half_row_sw128(uint8_t* tile, uint32_t row
 __device__ unsigned long long* g_trace;
 #define GDN_TRACE_AT(point, n)                                                      \
     do {                                                                            \
-        if (blockIdx.x == 0 && g_trace && (n) < 128) g_trace[(point) * 128 + (n)] = clock64(); \
+        if (tb_ && (n) < 128) tb_[(point) * 128 + (n)] = clock64(); \
     } while (0)
 #define GDN_TRACE_CTA(point)                                                        \
     do {                                                                            \
@@ -277,7 +255,7 @@ __device__ __forceinline__ void solve_block_row(int bi, uint32_t as_u, uint32_t 
 // n & 1): from X = [K; Q] K^T in TMEM, row r of A (rows 0-63, TMEM lanes
 // 0-63) or of P (lanes 64-127) per thread; gt = the thread's TMEM lane.
 __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float* gb, int n, int len, float scale,
-                                        int gt) {
+                                        int gt, unsigned long long* tb_) {
     using namespace tc;
     const int wq = gt >> 5;
     const int grp = n & 1;
@@ -363,6 +341,12 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     const int nc = (len + C - 1) / C;
     const int hk = h / p.grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef GDN_TRACE
+    unsigned long long* const tb_ = blockIdx.x == 0 ? g_trace : nullptr;  // traced block
+#else
+    unsigned long long* const tb_ = nullptr;
+    (void)tb_;
+#endif
     if (threadIdx.x == 0) GDN_TRACE_CTA(62);
 #ifdef GDN_TRACE
     if (threadIdx.x == 0 && g_trace && blockIdx.x < 128) {
@@ -400,6 +384,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (lane == 0) GDN_TRACE_AT(60, warp);
 
     auto kq_tile = [&](int n) { return sm + OFF_KQ + (uint32_t)(n % KQ_STAGES) * KQ_BYTES; };
     auto v_tile = [&](int n) { return sm + OFF_V + (uint32_t)(n % V_STAGES) * V_BYTES; };
@@ -636,7 +621,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (named_sync_or(bar_id, 128, !ok)) break;
             if (gt == 0) GDN_TRACE_AT(0, n);
             tc_fence_after();
-            ap_pass(sm, tmem, gb, n, len, p.scale, gt);
+            ap_pass(sm, tmem, gb, n, len, p.scale, gt, tb_);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_XFREE]);
@@ -730,13 +715,32 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (!WAITW(B_GB_FULL + m % GB_SLOTS, (m / GB_SLOTS) & 1) ||
                 !WAITW(B_XREADY0 + (m & 1), (m >> 1) & 1) || !WAITW(B_FULL_V + m % V_STAGES, (m / V_STAGES) & 1))
                 return false;
-            const float* gbm = gb_slot(m);
+            // 16-byte units u = ts + 256 k, k = 0..11: the K, Q stage (K kb0 | Q kb0
+            // | K kb1 | Q kb1, 512 units each: Q for k = 2, 3, 6, 7; tile row
+            // (ts >> 3) + 32 (k & 1)), then V (k = 8..11). Four loads before
+            // their stores in each group.
+            const float* qsc = gb_slot(m) + GB_QSC;
+            const float q0 = qsc[ts >> 3], q1 = qsc[(ts >> 3) + 32];
 #pragma unroll 1
-            for (int item = ts; item < 384; item += 256) {
-                const int t = item >> 7, rh = item & 127, r = rh & 63, kb = rh >> 6;
-                uint8_t* row = t == 2 ? v_tile(m) + (uint32_t)kb * 8192 + (uint32_t)r * 128
-                                      : kq_tile(m) + (uint32_t)kb * 16384 + (uint32_t)t * 8192 + (uint32_t)r * 128;
-                bf16_row_to_f16<true>(row, (uint32_t)r, t == 1 ? gbm[GB_QSC + r] : 1.f);
+            for (int i = 0; i < 3; ++i) {
+                uint4* base = i < 2 ? reinterpret_cast<uint4*>(kq_tile(m)) + 1024 * i : reinterpret_cast<uint4*>(v_tile(m));
+                uint4 u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[j] = base[ts + 256 * j];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w = u[j];
+                    if (j >= 2) {  // Q (i < 2) times gamma scale
+                        const float f = i < 2 ? (j == 2 ? q0 : q1) : 1.f;
+                        const float2 a = unbf2(w.x), b2 = unbf2(w.y), c = unbf2(w.z), d = unbf2(w.w);
+                        w.x = h2(a.x * f, a.y * f); w.y = h2(b2.x * f, b2.y * f);
+                        w.z = h2(c.x * f, c.y * f); w.w = h2(d.x * f, d.y * f);
+                    } else {
+                        const float2 a = unbf2(w.x), b2 = unbf2(w.y), c = unbf2(w.z), d = unbf2(w.w);
+                        w.x = h2(a.x, a.y); w.y = h2(b2.x, b2.y); w.z = h2(c.x, c.y); w.w = h2(d.x, d.y);
+                    }
+                    base[ts + 256 * j] = w;
+                }
             }
             fence_async_smem();
             __syncwarp();

@@ -13,6 +13,7 @@
 #pragma once
 
 #include "gdn_common.cuh"
+#include "gdn_epilogue.cuh"
 
 namespace gdn {
 
@@ -23,12 +24,17 @@ namespace gdn {
 // 64 contiguous bytes. The reductions over rows finish with 3 xor-shuffles
 // over the lane bits that select the row; no shared-memory reduction and no
 // block-wide barrier beyond the one that publishes k and q.
-template <typename TIn, typename TOut>
+// GATED: o is written through the epilogue of gdn_epilogue.cuh (zero-centred
+// RMSNorm over the 128 features of the head, times sigmoid(z)); its sum of
+// squares takes two more shuffles and one block barrier.
+template <typename TIn, typename TOut, bool GATED = false>
 __global__ void __launch_bounds__(256, 2)
 decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
                    const TIn* __restrict__ v, const float* __restrict__ g,
                    const float* __restrict__ beta, float* __restrict__ state,
-                   TOut* __restrict__ o, int h_qk, int h_v, int grp, float scale) {
+                   TOut* __restrict__ o, int h_qk, int h_v, int grp, float scale,
+                   const TIn* __restrict__ zg = nullptr, const float* __restrict__ wn = nullptr,
+                   float eps = 0.f) {
     constexpr int D = 128;
     const int nh = blockIdx.x;
     const int n = nh / h_v;
@@ -94,10 +100,35 @@ decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k,
         t.w = fmaf(a, s[m].w, ki * u[3]);
         __stcs(reinterpret_cast<float4*>(S + (size_t)(r0 + 8 * m) * D + col), t);
     }
+    float ov[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) ov[c] = scale * fmaf(a, qs[c], kq * u[c]);
+    if constexpr (GATED) {
+        // lanes with equal lane % 4 hold the same columns: the warp's 16
+        // columns are summed over lane bits 0-1, the 8 warps through smem
+        __shared__ float red[8];
+        float ss = ov[0] * ov[0] + ov[1] * ov[1] + ov[2] * ov[2] + ov[3] * ov[3];
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += red[i];
+        const float rinv = rsqrtf(fmaf(tot, 1.0f / D, eps));
+        if (r0 == 0) {
+            const TIn* zp = zg + (size_t)nh * D + col;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float sc = wn ? 1.0f + wn[col + c] : 1.0f;
+                ov[c] = ov[c] * rinv * sc * sigmoid_f(to_f32(zp[c]));
+            }
+        }
+    }
     if (r0 == 0) {
         TOut* op = o + (size_t)nh * D + col;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) op[c] = from_f32<TOut>(scale * fmaf(a, qs[c], kq * u[c]));
+        for (int c = 0; c < 4; ++c) op[c] = from_f32<TOut>(ov[c]);
     }
 }
 

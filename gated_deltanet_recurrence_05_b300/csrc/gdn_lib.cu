@@ -10,6 +10,7 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_epilogue.cuh"
 #include "gdn_decode.cuh"
 #include "gdn_chunk_simt.cuh"
 #include "gdn_chunk_tc.cuh"
@@ -46,21 +47,59 @@ gdn_status launch_simt(const gdn::SimtArgs& a, size_t smem, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// Epilogue over `rows` rows of d <= 1024 features (x, z may be different
+// dtypes; y may alias x when TY == TX).
+template <typename TX, typename TZ, typename TY>
+gdn_status launch_gated_rmsnorm(const void* x, const void* z, const float* w, void* y, long long rows, int d,
+                                float eps, cudaStream_t s) {
+    if (rows == 0) return GDN_OK;
+    const DevInfo di = dev_info();
+    const long long want = (rows + 7) / 8;
+    const long long cap = (long long)std::max(di.sms, 1) * 64;  // grid-strided beyond 64 CTAs per SM
+    const unsigned blocks = (unsigned)std::min(want, cap);
+    auto X = static_cast<const TX*>(x);
+    auto Z = static_cast<const TZ*>(z);
+    auto Y = static_cast<TY*>(y);
+    if (d == 128 && aligned(x, 16) && aligned(z, 16) && aligned(y, 16) && aligned(w, 16)) {
+        const long long groups = (rows + 3) / 4;  // 4 rows per warp, 8 warps per CTA
+        const unsigned b128 = (unsigned)std::min((groups + 7) / 8, cap);
+        gdn::gated_rmsnorm_d128_kernel<TX, TZ, TY><<<b128, 256, 0, s>>>(X, Z, w, Y, rows, eps);
+    } else if (d <= 128)
+        gdn::gated_rmsnorm_kernel<TX, TZ, TY, 4><<<blocks, 256, 0, s>>>(X, Z, w, Y, rows, d, eps);
+    else if (d <= 256)
+        gdn::gated_rmsnorm_kernel<TX, TZ, TY, 8><<<blocks, 256, 0, s>>>(X, Z, w, Y, rows, d, eps);
+    else if (d <= 512)
+        gdn::gated_rmsnorm_kernel<TX, TZ, TY, 16><<<blocks, 256, 0, s>>>(X, Z, w, Y, rows, d, eps);
+    else
+        gdn::gated_rmsnorm_kernel<TX, TZ, TY, 32><<<blocks, 256, 0, s>>>(X, Z, w, Y, rows, d, eps);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// z == nullptr: plain decode; otherwise o goes through the gated RMSNorm
+// epilogue (fused in the d = 128 kernel, a second launch elsewhere).
 template <typename TIn, typename TOut>
 gdn_status launch_decode(const void* q, const void* k, const void* v, const float* g,
                          const float* beta, float* state, void* o, int N, int h_qk, int h_v,
-                         int d_k, int d_v, float scale, cudaStream_t s) {
+                         int d_k, int d_v, float scale, cudaStream_t s,
+                         const void* z = nullptr, const float* w = nullptr, float eps = 0.f) {
     const long long blocks = (long long)N * h_v;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     const int grp = h_v / h_qk;
     if (d_k == 128 && d_v == 128) {
-        gdn::decode_d128_kernel<TIn, TOut><<<(unsigned)blocks, 256, 0, s>>>(
-            static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
-            state, static_cast<TOut*>(o), h_qk, h_v, grp, scale);
+        if (z)
+            gdn::decode_d128_kernel<TIn, TOut, true><<<(unsigned)blocks, 256, 0, s>>>(
+                static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
+                state, static_cast<TOut*>(o), h_qk, h_v, grp, scale, static_cast<const TIn*>(z), w, eps);
+        else
+            gdn::decode_d128_kernel<TIn, TOut><<<(unsigned)blocks, 256, 0, s>>>(
+                static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
+                state, static_cast<TOut*>(o), h_qk, h_v, grp, scale);
     } else {
         gdn::decode_generic_kernel<TIn, TOut><<<(unsigned)blocks, 128, 0, s>>>(
             static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta,
             state, static_cast<TOut*>(o), h_qk, h_v, grp, d_k, d_v, scale);
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+        if (z) return launch_gated_rmsnorm<TOut, TIn, TOut>(o, z, w, o, blocks, d_v, eps, s);
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
@@ -80,7 +119,7 @@ const char* gdn_status_string(gdn_status s) {
     return "GDN_ERR_UNKNOWN";
 }
 
-int32_t gdn_version(void) { return 100; }
+int32_t gdn_version(void) { return 101; }
 
 gdn_status gdn_plan_seq_order(const int32_t* cu, int32_t num_seqs, int32_t* order_out) {
     if (num_seqs < 0 || (num_seqs > 0 && (cu == nullptr || order_out == nullptr))) return GDN_ERR_INVALID_ARG;
@@ -106,29 +145,68 @@ gdn_status gdn_get_device_error(void* stream, uint32_t* code) {
     return GDN_OK;
 }
 
-gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
-                           const float* beta, float* state, void* o, int32_t num_seqs,
-                           int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
-                           int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream) {
+gdn_status gdn_decode_step_gated(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, float* state, void* o, const void* gate,
+                                 const float* norm_weight, float eps, int32_t num_seqs,
+                                 int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                                 int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream) {
     if (num_seqs < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
         return GDN_ERR_INVALID_ARG;
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return GDN_OK;
     const uintptr_t ei = esize(dtype_qkv), eo = esize(dtype_o);
     if (!ok_ptr(q, ei) || !ok_ptr(k, ei) || !ok_ptr(v, ei) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) ||
-        !ok_ptr(state, 16) || !ok_ptr(o, eo))
+        !ok_ptr(state, 16) || !ok_ptr(o, eo) || !ok_opt(gate, ei) || !ok_opt(norm_weight, 4))
         return GDN_ERR_INVALID_ARG;
+    if (gate == nullptr && norm_weight != nullptr) return GDN_ERR_INVALID_ARG;
     if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool bf_in = dtype_qkv == GDN_BF16, bf_out = dtype_o == GDN_BF16;
     if (bf_in && bf_out)
-        return launch_decode<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+        return launch_decode<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k,
+                                                           d_v, scale, s, gate, norm_weight, eps);
     if (bf_in)
-        return launch_decode<__nv_bfloat16, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+        return launch_decode<__nv_bfloat16, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v,
+                                                   scale, s, gate, norm_weight, eps);
     if (bf_out)
-        return launch_decode<float, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
-    return launch_decode<float, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s);
+        return launch_decode<float, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v,
+                                                   scale, s, gate, norm_weight, eps);
+    return launch_decode<float, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, d_k, d_v, scale, s,
+                                       gate, norm_weight, eps);
+}
+
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, void* o, int32_t num_seqs,
+                           int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                           int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream) {
+    return gdn_decode_step_gated(q, k, v, g, beta, state, o, nullptr, nullptr, 0.f, num_seqs, h_qk, h_v, d_k,
+                                 d_v, dtype_qkv, dtype_o, scale, stream);
+}
+
+gdn_status gdn_gated_rmsnorm(const void* x, const void* gate, const float* norm_weight, void* y, int64_t rows,
+                             int32_t d, int32_t dtype_x, int32_t dtype_y, float eps, void* stream) {
+    if (rows < 0 || d <= 0) return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_x) || !ok_dtype(dtype_y)) return GDN_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || !isfinite(eps)) return GDN_ERR_INVALID_ARG;
+    if (d > 1024) return GDN_ERR_UNSUPPORTED;
+    if (rows == 0) return GDN_OK;
+    const uintptr_t ex = esize(dtype_x), ey = esize(dtype_y);
+    if (!ok_ptr(x, ex) || !ok_ptr(gate, ex) || !ok_opt(norm_weight, 4) || !ok_ptr(y, ey))
+        return GDN_ERR_INVALID_ARG;
+    // in place only with equal element types (each row is read before it is written)
+    if (y == x && dtype_x != dtype_y) return GDN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bx = dtype_x == GDN_BF16, by = dtype_y == GDN_BF16;
+    if (bx && by)
+        return launch_gated_rmsnorm<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(x, gate, norm_weight, y, rows, d,
+                                                                                 eps, s);
+    if (bx)
+        return launch_gated_rmsnorm<__nv_bfloat16, __nv_bfloat16, float>(x, gate, norm_weight, y, rows, d, eps, s);
+    if (by)
+        return launch_gated_rmsnorm<float, float, __nv_bfloat16>(x, gate, norm_weight, y, rows, d, eps, s);
+    return launch_gated_rmsnorm<float, float, float>(x, gate, norm_weight, y, rows, d, eps, s);
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,

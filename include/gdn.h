@@ -130,6 +130,55 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v,
                            void* stream);
 
 /*
+ * gdn_gated_rmsnorm -- output epilogue of a GDN layer, per row of d features:
+ *
+ *     y = x / sqrt(mean_j x_j^2 + eps) * (1 + w) * sigmoid(gate)
+ *
+ * (zero-centred RMSNorm, then the sigmoid output gate; the pages name both:
+ * "a sigmoid output gate, zero-centered RMSNorm", podcast episode
+ * "Qwen3.8-Next design: hybrid attention, residuals and n-gram embeddings",
+ * transcript segment 14, and the gate sigma(x W_g) (.) o in the component list
+ * of the page "Qwen3.8 attention gate". The order, the zero-centred weight and
+ * eps are this library's reading: norm first, scale 1 + w, eps inside the root.)
+ *
+ * x, gate     [rows, d] dtype_x   (for a GDN output: rows = T_total * H_v,
+ *                                   d = d_v; gate = the caller's x W_g)
+ * norm_weight [d] fp32, shared by all rows; NULL = 0 (scale 1)
+ * y           [rows, d] dtype_y (written). y == x (in place) is allowed when
+ *             dtype_y == dtype_x; other overlaps are not.
+ * eps         >= 0 and finite (1e-6 is the usual value)
+ *
+ * One warp per row, one read of x and gate and one write of y (HBM-bound).
+ * Returns GDN_ERR_INVALID_ARG for null/misaligned pointers (element size;
+ * 4 bytes for norm_weight), rows < 0, d < 1, a bad code, a bad eps or an
+ * in-place call with differing dtypes; GDN_ERR_UNSUPPORTED for d > 1024.
+ */
+gdn_status gdn_gated_rmsnorm(const void* x, const void* gate, const float* norm_weight, void* y,
+                             int64_t rows, int32_t d, int32_t dtype_x, int32_t dtype_y,
+                             float eps, void* stream);
+
+/*
+ * gdn_decode_step_gated -- gdn_decode_step whose output goes through the
+ * epilogue of gdn_gated_rmsnorm (per sequence and value head, over the d_v
+ * features): o = rmsnorm(S'^T q scale) * (1 + norm_weight) * sigmoid(gate).
+ *
+ * gate        [N, H_v, d_v] dtype_qkv; NULL = no epilogue (the plain step)
+ * norm_weight [d_v] fp32, NULL = 0; must be NULL when gate is NULL
+ * eps         >= 0 and finite
+ * Other arguments and errors as for gdn_decode_step. With d_k = d_v = 128 the
+ * epilogue is fused into the decode kernel (the output never round-trips
+ * through memory); other sizes run it as a second launch on o.
+ */
+gdn_status gdn_decode_step_gated(const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta,
+                                 float* state, void* o, const void* gate,
+                                 const float* norm_weight, float eps,
+                                 int32_t num_seqs, int32_t h_qk, int32_t h_v,
+                                 int32_t d_k, int32_t d_v,
+                                 int32_t dtype_qkv, int32_t dtype_o, float scale,
+                                 void* stream);
+
+/*
  * gdn_plan_seq_order -- HOST helper: writes into order_out[0..N-1] (host
  * memory) the sequence indices sorted by length, longest first (ties keep
  * index order), from a HOST copy of cu_seqlens [N + 1]. The caller copies the

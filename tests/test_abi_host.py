@@ -34,7 +34,8 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_plan_seq_order",
+    for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
+                 "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
         assert need in names
 
@@ -135,3 +136,49 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(ImportError):
         gdn.lib()
+
+
+def _norm(L, **kw):
+    a = dict(x=FAKE, z=FAKE, w=None, y=FAKE + 0x1000, rows=8, d=128, dx=1, dy=1, eps=1e-6)
+    a.update(kw)
+    return L.gdn_gated_rmsnorm(a["x"], a["z"], a["w"], a["y"], a["rows"], a["d"], a["dx"], a["dy"], a["eps"],
+                               None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), INVALID),
+    (dict(z=None), INVALID),
+    (dict(y=None), INVALID),
+    (dict(x=FAKE + 1), INVALID),                 # bf16 needs 2-byte alignment
+    (dict(w=FAKE + 2), INVALID),                 # the fp32 weight needs 4 bytes
+    (dict(rows=-1), INVALID),
+    (dict(d=0), INVALID),
+    (dict(dx=7), INVALID),
+    (dict(eps=-1.0), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(y=FAKE, dy=0), INVALID),               # in place needs equal dtypes
+    (dict(d=1025), UNSUPPORTED),
+    (dict(rows=0), OK),                          # nothing to do, nothing launched
+])
+def test_gated_rmsnorm_host_validation(L, kw, status):
+    assert _norm(L, **kw) == status
+
+
+def _dec_gated(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, S=FAKE, o=FAKE, z=FAKE, w=None, eps=1e-6, N=2, h_qk=1,
+             h_v=2, d_k=128, d_v=128, dq=1, do=1, scale=0.0)
+    a.update(kw)
+    return L.gdn_decode_step_gated(a["q"], a["k"], a["v"], a["g"], a["beta"], a["S"], a["o"], a["z"], a["w"],
+                                   a["eps"], a["N"], a["h_qk"], a["h_v"], a["d_k"], a["d_v"], a["dq"], a["do"],
+                                   a["scale"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(z=FAKE + 1), INVALID),                 # the gate takes the q/k/v dtype alignment
+    (dict(z=None, w=FAKE), INVALID),             # a weight without a gate
+    (dict(eps=-0.5), INVALID),
+    (dict(d_v=129), UNSUPPORTED),
+    (dict(N=0), OK),
+])
+def test_decode_gated_host_validation(L, kw, status):
+    assert _dec_gated(L, **kw) == status
