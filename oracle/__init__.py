@@ -12,6 +12,8 @@ numpy / torch CPU arrays into it and back.
   chunked(...)    the chunkwise algebra, used only to pin that algebra
   gated_rmsnorm(...)  the output epilogue (zero-centred RMSNorm times a
                   sigmoid gate), numpy fp64, in ``epilogue.py``
+  short_conv(...), short_conv_step(...)  the input prologue (causal
+                  depthwise conv, SiLU, per-head L2 norm), in ``prologue.py``
 
 Both return ``(o, S)``: with ``pairs=None`` o is [T_total, H_v, d_v] and S is
 [N, H_v, d_k, d_v] (float64 numpy); with ``pairs=[(n, h), ...]`` they are
@@ -31,6 +33,7 @@ import threading
 import numpy as np
 
 from .epilogue import gated_rmsnorm, rms_normalize, sigmoid  # noqa: F401
+from .prologue import l2_normalize_groups, short_conv, short_conv_step, silu  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
