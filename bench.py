@@ -308,6 +308,7 @@ def run_ours(args, world, rank, local):
 
     decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
     epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o)
+    prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -324,7 +325,7 @@ def run_ours(args, world, rank, local):
                    "global_batch": N * world, "seq_len": T // N, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (126 MB) every step; no flush"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
-        "clocks": clk.summary(), "decode": decode, "epilogue": epilogue,
+        "clocks": clk.summary(), "decode": decode, "epilogue": epilogue, "prologue": prologue,
     }
 
 
@@ -435,6 +436,49 @@ def run_epilogue(args, dev, peaks, world, o):
     return out
 
 
+def run_prologue(args, dev, peaks, world, w):
+    """The GDN input prologue (causal depthwise conv K=4, silu, per-head L2 norm
+    for q and k) on the three projections of the prefill workload."""
+    import gated_deltanet_recurrence_05_b300 as gdn
+    T = sum(w["lengths"])
+    N = len(w["lengths"])
+    gen = torch.Generator().manual_seed(args.seed + 77)
+    shapes = [(w["h_qk"] * w["d_k"], w["d_k"]), (w["h_qk"] * w["d_k"], w["d_k"]), (w["h_v"] * w["d_v"], 0)]
+    bufs = []
+    for C, ng in shapes:
+        x = torch.randn(T, C, generator=gen).to(torch.bfloat16).to(dev)
+        wt = (torch.randn(C, 4, generator=gen) * 0.5).to(dev)
+        bufs.append((x, wt, torch.empty_like(x), ng))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for x, wt, y, ng in bufs:
+            gdn.short_conv(x, wt, cu_seqlens=w["cu_seqlens"].to(dev) if w["cu_seqlens"] is not None else None,
+                           num_seqs=N, norm_group=ng, out=y, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    reps = max(3, args.steps)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(reps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if gdn.get_device_error() != 0:
+        raise RuntimeError("device error in the prologue")
+    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+    b = sum(2 * x.numel() * x.element_size() + wt.numel() * 4 for x, wt, _, _ in bufs)
+    gbs = b / (us / 1e6) / 1e9
+    return {"workload": f"short conv (K=4) + silu (+ L2 norm per head for q, k) on the q, k [{T}, "
+                        f"{shapes[0][0]}] and v [{T}, {shapes[2][0]}] bf16 projections of the prefill workload",
+            "us_per_step": us, "GB_per_s": gbs * world, "gpu_launches": 3 * reps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
+
+
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores (bounded sample)."""
     if rank != 0:
@@ -473,7 +517,7 @@ def main(argv=None):
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the prefill kernel from an ncu capture")
     ap.add_argument("--skip-decode", action="store_true")
-    ap.add_argument("--skip-epilogue", action="store_true")
+    ap.add_argument("--skip-epilogue", action="store_true", help="skip the epilogue and prologue lines")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

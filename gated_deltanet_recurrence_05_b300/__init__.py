@@ -61,6 +61,10 @@ def lib():
         L.gdn_decode_step_gated.restype = ctypes.c_int
         L.gdn_gated_rmsnorm.argtypes = [P, P, P, P, I64, I32, I32, I32, F, P]
         L.gdn_gated_rmsnorm.restype = ctypes.c_int
+        L.gdn_short_conv.argtypes = [P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, P]
+        L.gdn_short_conv.restype = ctypes.c_int
+        L.gdn_short_conv_step.argtypes = [P, P, P, P, I32, I32, I32, I32, F, I32, P]
+        L.gdn_short_conv_step.restype = ctypes.c_int
         L.gdn_plan_seq_order.argtypes = [P, I32, P]
         L.gdn_plan_seq_order.restype = ctypes.c_int
         L.gdn_get_device_error.argtypes = [P, P]
@@ -223,3 +227,52 @@ def get_device_error(stream=None) -> int:
     code = ctypes.c_uint32(0)
     _check("gdn_get_device_error", lib().gdn_get_device_error(_stream(stream), ctypes.byref(code)))
     return int(code.value)
+
+
+def short_conv(x: torch.Tensor, w: torch.Tensor, *, cu_seqlens: Optional[torch.Tensor] = None,
+               num_seqs: Optional[int] = None, conv_state: Optional[torch.Tensor] = None,
+               return_final_state: bool = False, norm_group: int = 0, eps: float = 1e-6,
+               out: Optional[torch.Tensor] = None, stream=None):
+    """GDN input prologue on one projected tensor: causal depthwise conv over the
+    tokens of each sequence, silu, and (norm_group > 0) an L2 norm per head.
+
+    x: [T, C] or [T, H, d] (C = H d); w: [C, K] fp32, K <= 4; cu_seqlens: [N + 1]
+    int32 (CUDA) or None with ``num_seqs`` equal-length sequences (default 1);
+    conv_state: [N, C, K - 1] fp32, the inputs preceding each sequence. Returns y
+    (shape of x) and, with ``return_final_state``, the [N, C, K - 1] final state.
+    """
+    _dev(x, "x")
+    _dev(w, "w")
+    T = x.shape[0]
+    C = x.numel() // T if T else int(w.shape[0])
+    K = int(w.shape[1])
+    if cu_seqlens is not None:
+        _dev(cu_seqlens, "cu_seqlens")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    if conv_state is not None:
+        _dev(conv_state, "conv_state")
+    y = out if out is not None else torch.empty_like(x)
+    fs = torch.empty(N, C, K - 1, dtype=torch.float32, device=x.device) if return_final_state else None
+    st = lib().gdn_short_conv(_ptr(x), _ptr(w), _ptr(y), _ptr(cu_seqlens), _ptr(conv_state), _ptr(fs), N, T, C, K,
+                              int(norm_group), float(eps), _code(x), _stream(stream))
+    _check("gdn_short_conv", st)
+    return (y, fs) if return_final_state else y
+
+
+def short_conv_step(x: torch.Tensor, w: torch.Tensor, conv_state: torch.Tensor, *, norm_group: int = 0,
+                    eps: float = 1e-6, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The prologue for one token per sequence (decode): x [N, C] or [N, H, d];
+    ``conv_state`` [N, C, K - 1] fp32 is shifted in place. Returns y (shape of x)."""
+    _dev(x, "x")
+    _dev(w, "w")
+    _dev(conv_state, "conv_state")
+    N = x.shape[0]
+    C = x.numel() // N if N else int(w.shape[0])
+    y = out if out is not None else torch.empty_like(x)
+    st = lib().gdn_short_conv_step(_ptr(x), _ptr(w), _ptr(conv_state), _ptr(y), N, C, int(w.shape[1]),
+                                   int(norm_group), float(eps), _code(x), _stream(stream))
+    _check("gdn_short_conv_step", st)
+    return y
+

@@ -23,9 +23,7 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// sigmoid(z) = 1 / (1 + e^-z): exactly 0 (not NaN) for very negative z and 1
-// for very positive z.
-__device__ __forceinline__ float sigmoid_f(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f(float z) { return sigmoid_fast(z); }
 
 // Rows r = blockIdx.x * 8 + warp (grid-strided); lane l owns features
 // l + 32 m, m < NV (NV = the smallest of 4, 8, 16, 32 with 32 NV >= d).
@@ -90,7 +88,8 @@ gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __
                           long long rows, float eps) {
     constexpr int D = 128, R = 4;
     const int lane = threadIdx.x & 31;
-    const float4 wv = w ? *reinterpret_cast<const float4*>(w + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 ws = w ? *reinterpret_cast<const float4*>(w + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ws.x += 1.0f; ws.y += 1.0f; ws.z += 1.0f; ws.w += 1.0f;  // zero-centred weight -> scale
     const long long warps = (long long)gridDim.x * 8;
     for (long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R; r0 < rows; r0 += warps * R) {
         float4 xv[R], zv[R];
@@ -114,10 +113,10 @@ gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __
             if (r0 + i >= rows) break;
             const float rinv = rsqrtf(fmaf(ss[i], 1.0f / D, eps));
             float4 o;
-            o.x = xv[i].x * rinv * (1.0f + wv.x) * sigmoid_f(zv[i].x);
-            o.y = xv[i].y * rinv * (1.0f + wv.y) * sigmoid_f(zv[i].y);
-            o.z = xv[i].z * rinv * (1.0f + wv.z) * sigmoid_f(zv[i].z);
-            o.w = xv[i].w * rinv * (1.0f + wv.w) * sigmoid_f(zv[i].w);
+            o.x = xv[i].x * (rinv * ws.x) * sigmoid_f(zv[i].x);
+            o.y = xv[i].y * (rinv * ws.y) * sigmoid_f(zv[i].y);
+            o.z = xv[i].z * (rinv * ws.z) * sigmoid_f(zv[i].z);
+            o.w = xv[i].w * (rinv * ws.w) * sigmoid_f(zv[i].w);
             store4(y + (r0 + i) * D + 4 * lane, o);
         }
     }

@@ -11,6 +11,7 @@
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_epilogue.cuh"
+#include "gdn_prologue.cuh"
 #include "gdn_decode.cuh"
 #include "gdn_chunk_simt.cuh"
 #include "gdn_chunk_tc.cuh"
@@ -55,7 +56,7 @@ gdn_status launch_gated_rmsnorm(const void* x, const void* z, const float* w, vo
     if (rows == 0) return GDN_OK;
     const DevInfo di = dev_info();
     const long long want = (rows + 7) / 8;
-    const long long cap = (long long)std::max(di.sms, 1) * 64;  // grid-strided beyond 64 CTAs per SM
+    const long long cap = (long long)std::max(di.sms, 1) * 8;  // one resident wave, grid-strided
     const unsigned blocks = (unsigned)std::min(want, cap);
     auto X = static_cast<const TX*>(x);
     auto Z = static_cast<const TZ*>(z);
@@ -102,6 +103,67 @@ gdn_status launch_decode(const void* q, const void* k, const void* v, const floa
         if (z) return launch_gated_rmsnorm<TOut, TIn, TOut>(o, z, w, o, blocks, d_v, eps, s);
     }
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename T, int K>
+gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32_t* cu, const float* st_in,
+                             float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s) {
+    const DevInfo di = dev_info();
+    const long long runs = (total + 31) / 32;  // 32 tokens per warp
+    const int cblocks = (C + 127) / 128;
+    if (runs > 0) {
+        if (cblocks > 65535) return GDN_ERR_UNSUPPORTED;
+        const long long cap = std::max(1LL, (long long)std::max(di.sms, 1) * 8 / cblocks);  // one wave
+        const dim3 grid((unsigned)std::min((runs + 7) / 8, cap), (unsigned)cblocks);
+        const long long eq = cu ? 0 : total / N;
+        gdn::short_conv_kernel<T, K><<<grid, 256, 0, s>>>(static_cast<const T*>(x), w, static_cast<T*>(y), cu,
+                                                           st_in, st_out, N, total, eq, C, ng, eps);
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    if (st_out && (cu || total == 0) && K > 1) {  // empty sequences carry their state over
+        const long long n = (long long)N * C * (K - 1);
+        gdn::conv_state_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cu, st_in, st_out, N,
+                                                                                  (long long)C * (K - 1));
+    }
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename T, int K>
+gdn_status launch_short_conv_step(const void* x, const float* w, float* st, void* y, int N, int C, int ng,
+                                  float eps, cudaStream_t s) {
+    const DevInfo di = dev_info();
+    const long long units = (long long)N * ((C + 127) / 128);
+    const long long cap = (long long)std::max(di.sms, 1) * 64;
+    const unsigned blocks = (unsigned)std::min((units + 7) / 8, cap);
+    gdn::short_conv_step_kernel<T, K><<<blocks, 256, 0, s>>>(static_cast<const T*>(x), w, st, static_cast<T*>(y), N,
+                                                              C, ng, eps);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename T>
+gdn_status dispatch_conv(int K, const void* x, const float* w, void* y, const int32_t* cu, const float* st_in,
+                         float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s) {
+    switch (K) {
+        case 1: return launch_short_conv<T, 1>(x, w, y, cu, st_in, st_out, N, total, C, ng, eps, s);
+        case 2: return launch_short_conv<T, 2>(x, w, y, cu, st_in, st_out, N, total, C, ng, eps, s);
+        case 3: return launch_short_conv<T, 3>(x, w, y, cu, st_in, st_out, N, total, C, ng, eps, s);
+        default: return launch_short_conv<T, 4>(x, w, y, cu, st_in, st_out, N, total, C, ng, eps, s);
+    }
+}
+
+template <typename T>
+gdn_status dispatch_conv_step(int K, const void* x, const float* w, float* st, void* y, int N, int C, int ng,
+                              float eps, cudaStream_t s) {
+    switch (K) {
+        case 1: return launch_short_conv_step<T, 1>(x, w, st, y, N, C, ng, eps, s);
+        case 2: return launch_short_conv_step<T, 2>(x, w, st, y, N, C, ng, eps, s);
+        case 3: return launch_short_conv_step<T, 3>(x, w, st, y, N, C, ng, eps, s);
+        default: return launch_short_conv_step<T, 4>(x, w, st, y, N, C, ng, eps, s);
+    }
+}
+
+bool ok_norm_group(int ng, int C) {
+    return ng == 0 || ((ng == 4 || ng == 8 || ng == 16 || ng == 32 || ng == 64 || ng == 128) && C % ng == 0);
 }
 
 }  // namespace
@@ -207,6 +269,45 @@ gdn_status gdn_gated_rmsnorm(const void* x, const void* gate, const float* norm_
     if (by)
         return launch_gated_rmsnorm<float, float, __nv_bfloat16>(x, gate, norm_weight, y, rows, d, eps, s);
     return launch_gated_rmsnorm<float, float, float>(x, gate, norm_weight, y, rows, d, eps, s);
+}
+
+gdn_status gdn_short_conv(const void* x, const float* w, void* y, const int32_t* cu_seqlens,
+                          const float* conv_state_in, float* conv_state_out, int32_t num_seqs,
+                          int64_t total_tokens, int32_t channels, int32_t kernel_size, int32_t norm_group,
+                          float eps, int32_t dtype, void* stream) {
+    if (num_seqs < 0 || total_tokens < 0 || channels <= 0 || kernel_size < 1) return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype) || !(eps >= 0.f) || !isfinite(eps)) return GDN_ERR_INVALID_ARG;
+    if (channels % 4 != 0 || !ok_norm_group(norm_group, channels)) return GDN_ERR_INVALID_ARG;
+    if (kernel_size > 4) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
+    if (!ok_ptr(x) || !ok_ptr(w, 4) || !ok_ptr(y) || !ok_opt(cu_seqlens, 4) || !ok_opt(conv_state_in, 4) ||
+        !ok_opt(conv_state_out, 4))
+        return GDN_ERR_INVALID_ARG;
+    if (y == x) return GDN_ERR_INVALID_ARG;  // the taps read neighbours: no in-place
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GDN_BF16)
+        return dispatch_conv<__nv_bfloat16>(kernel_size, x, w, y, cu_seqlens, conv_state_in, conv_state_out, num_seqs,
+                                            total_tokens, channels, norm_group, eps, s);
+    return dispatch_conv<float>(kernel_size, x, w, y, cu_seqlens, conv_state_in, conv_state_out, num_seqs,
+                                total_tokens, channels, norm_group, eps, s);
+}
+
+gdn_status gdn_short_conv_step(const void* x, const float* w, float* conv_state, void* y, int32_t num_seqs,
+                               int32_t channels, int32_t kernel_size, int32_t norm_group, float eps, int32_t dtype,
+                               void* stream) {
+    if (num_seqs < 0 || channels <= 0 || kernel_size < 1) return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype) || !(eps >= 0.f) || !isfinite(eps)) return GDN_ERR_INVALID_ARG;
+    if (channels % 4 != 0 || !ok_norm_group(norm_group, channels)) return GDN_ERR_INVALID_ARG;
+    if (kernel_size > 4) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return GDN_OK;
+    if (!ok_ptr(x) || !ok_ptr(w, 4) || !ok_ptr(y) || (kernel_size > 1 && !ok_ptr(conv_state, 4)))
+        return GDN_ERR_INVALID_ARG;
+    if (y == x) return GDN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == GDN_BF16)
+        return dispatch_conv_step<__nv_bfloat16>(kernel_size, x, w, conv_state, y, num_seqs, channels, norm_group, eps, s);
+    return dispatch_conv_step<float>(kernel_size, x, w, conv_state, y, num_seqs, channels, norm_group, eps, s);
 }
 
 gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,

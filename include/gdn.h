@@ -179,6 +179,50 @@ gdn_status gdn_decode_step_gated(const void* q, const void* k, const void* v,
                                  void* stream);
 
 /*
+ * gdn_short_conv -- input prologue of a GDN layer on one projected tensor
+ * (q, k or v): a short causal depthwise convolution over the tokens of each
+ * sequence, then SiLU, then (norm_group > 0) an L2 norm per head:
+ *
+ *     u[t, c] = sum_{i<K} w[c, i] * x[t - (K-1) + i, c]
+ *     y[t, c] = silu(u[t, c]) / sqrt(sum over c's head of silu(u)^2 + eps)
+ *
+ * (the pages: GDN adds "short causal convolutions", podcast episode
+ * "Qwen3.8-Next design: hybrid attention, residuals and n-gram embeddings",
+ * transcript segment 14; q and k enter the recurrence L2-normalised. The tap
+ * order, the state convention and eps are this library's reading.)
+ *
+ * x, y            [T_total, C] dtype (y written; y must not overlap x)
+ * w               [C, K] fp32; tap K-1 multiplies the current token
+ * cu_seqlens      [N + 1] int32 device array, or NULL = N sequences of equal
+ *                 length (as for gdn_chunk_fwd)
+ * conv_state_in   [N, C, K-1] fp32: the K-1 inputs that preceded each
+ *                 sequence, oldest first; NULL = zeros
+ * conv_state_out  [N, C, K-1] fp32 (written): the last K-1 inputs of each
+ *                 sequence (older state entries when it is shorter); NULL =
+ *                 not written. Must not overlap conv_state_in.
+ * kernel_size     1..4 (GDN_ERR_UNSUPPORTED above)
+ * norm_group      0 (no norm: v) or the head size of q/k: 4, 8, ..., 128,
+ *                 dividing C
+ * C               a multiple of 4; x and y 16-byte aligned
+ *
+ * One warp per (token, 128 channels), one read of x from DRAM and one write
+ * of y. Errors as for gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG for y == x.
+ */
+gdn_status gdn_short_conv(const void* x, const float* w, void* y, const int32_t* cu_seqlens,
+                          const float* conv_state_in, float* conv_state_out, int32_t num_seqs,
+                          int64_t total_tokens, int32_t channels, int32_t kernel_size,
+                          int32_t norm_group, float eps, int32_t dtype, void* stream);
+
+/*
+ * gdn_short_conv_step -- the prologue for one token per sequence (decode):
+ * x, y [N, C] dtype; conv_state [N, C, K-1] fp32, read and shifted in place
+ * (the token becomes its newest entry). Other arguments as gdn_short_conv.
+ */
+gdn_status gdn_short_conv_step(const void* x, const float* w, float* conv_state, void* y,
+                               int32_t num_seqs, int32_t channels, int32_t kernel_size,
+                               int32_t norm_group, float eps, int32_t dtype, void* stream);
+
+/*
  * gdn_plan_seq_order -- HOST helper: writes into order_out[0..N-1] (host
  * memory) the sequence indices sorted by length, longest first (ties keep
  * index order), from a HOST copy of cu_seqlens [N + 1]. The caller copies the

@@ -35,6 +35,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
+                 "gdn_short_conv", "gdn_short_conv_step",
                  "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
         assert need in names
@@ -182,3 +183,39 @@ def _dec_gated(L, **kw):
 ])
 def test_decode_gated_host_validation(L, kw, status):
     assert _dec_gated(L, **kw) == status
+
+
+def _conv(L, **kw):
+    a = dict(x=FAKE, w=FAKE, y=FAKE + 0x1000, cu=None, s_in=None, s_out=None, N=2, T=64, C=256, K=4, ng=128,
+             eps=1e-6, dt=1)
+    a.update(kw)
+    return L.gdn_short_conv(a["x"], a["w"], a["y"], a["cu"], a["s_in"], a["s_out"], a["N"], a["T"], a["C"], a["K"],
+                            a["ng"], a["eps"], a["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), INVALID),
+    (dict(w=FAKE + 2), INVALID),
+    (dict(y=FAKE), INVALID),                     # no in-place: the taps read neighbours
+    (dict(C=130), INVALID),                      # C % 4
+    (dict(ng=48), INVALID),                      # not a power-of-two divisor of 128
+    (dict(C=192, ng=128), INVALID),              # C % norm_group
+    (dict(T=63), INVALID),                       # equal lengths need T % N == 0
+    (dict(N=0, T=64), INVALID),
+    (dict(K=0), INVALID),
+    (dict(K=5), UNSUPPORTED),
+    (dict(eps=-1.0), INVALID),
+    (dict(N=0, T=0), OK),
+])
+def test_short_conv_host_validation(L, kw, status):
+    assert _conv(L, **kw) == status
+
+
+def test_short_conv_step_host_validation(L):
+    call = lambda **kw: L.gdn_short_conv_step(kw.get("x", FAKE), kw.get("w", FAKE), kw.get("s", FAKE),
+                                              kw.get("y", FAKE + 0x1000), kw.get("N", 2), kw.get("C", 256),
+                                              kw.get("K", 4), kw.get("ng", 0), kw.get("eps", 1e-6), 1, None)
+    assert call(s=None) == INVALID
+    assert call(y=FAKE) == INVALID
+    assert call(K=5) == UNSUPPORTED
+    assert call(N=0) == OK
