@@ -16,16 +16,6 @@ __device__ __forceinline__ void set_device_error(unsigned int bits) {
     atomicOr(&g_device_error, bits);
 }
 
-// sigmoid(z) = 1 / (1 + 2^(-z log2 e)) on the special-function unit (PTX
-// ex2.approx.ftz and rcp.approx.ftz, each within a few ulp): exactly 0 for
-// z -> -inf (the reciprocal of +inf) and 1 for z -> +inf.
-__device__ __forceinline__ float sigmoid_fast(float z) {
-    float e, r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * z));
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
-    return r;
-}
-
 // Element loads/stores for the two storage dtypes.
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

@@ -23,6 +23,15 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// sigmoid(z) = 1 / (1 + 2^(-z log2 e)) on the special-function unit (PTX
+// ex2.approx.ftz and rcp.approx.ftz, each within a few ulp): exactly 0 for
+// z -> -inf (the reciprocal of +inf) and 1 for z -> +inf.
+__device__ __forceinline__ float sigmoid_fast(float z) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * z));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return r;
+}
 __device__ __forceinline__ float sigmoid_f(float z) { return sigmoid_fast(z); }
 
 // Rows r = blockIdx.x * 8 + warp (grid-strided); lane l owns features
@@ -82,6 +91,25 @@ __device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<f
 // d = 128 with 16-byte aligned bases: lane l owns features 4l .. 4l + 3 of a
 // row (one vector load of x and of z), and each warp keeps R = 4 rows in
 // flight so that enough bytes are outstanding per SM to reach HBM bandwidth.
+// Raw 4-element vectors (kept packed until used: fewer registers, more rows
+// in flight per SM).
+template <typename T> struct Vec4;
+template <> struct Vec4<__nv_bfloat16> { using type = uint2; };
+template <> struct Vec4<float> { using type = float4; };
+template <typename T>
+__device__ __forceinline__ typename Vec4<T>::type load_raw4(const T* p) {
+    return *reinterpret_cast<const typename Vec4<T>::type*>(p);
+}
+__device__ __forceinline__ float4 unpack4(uint2 u) {
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ float4 unpack4(float4 f) { return f; }
+
+// d = 128 with 16-byte aligned bases: lane l owns features 4l .. 4l + 3 of a
+// row (one vector load of x and of z), and each warp keeps R = 4 rows in
+// flight (raw vectors until used) so that enough bytes are outstanding per SM
+// to reach HBM bandwidth.
 template <typename TX, typename TZ, typename TY>
 __global__ void __launch_bounds__(256)
 gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __restrict__ w, TY* y,
@@ -92,17 +120,20 @@ gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __
     ws.x += 1.0f; ws.y += 1.0f; ws.z += 1.0f; ws.w += 1.0f;  // zero-centred weight -> scale
     const long long warps = (long long)gridDim.x * 8;
     for (long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R; r0 < rows; r0 += warps * R) {
-        float4 xv[R], zv[R];
-        float ss[R];
+        typename Vec4<TX>::type xr[R];
+        typename Vec4<TZ>::type zr[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const long long row = r0 + i < rows ? r0 + i : rows - 1;  // tail rows repeat the last row
-            xv[i] = load4(x + row * D + 4 * lane);
-            zv[i] = load4(z + row * D + 4 * lane);
+            xr[i] = load_raw4(x + row * D + 4 * lane);
+            zr[i] = load_raw4(z + row * D + 4 * lane);
         }
+        float ss[R];
 #pragma unroll
-        for (int i = 0; i < R; ++i)
-            ss[i] = xv[i].x * xv[i].x + xv[i].y * xv[i].y + xv[i].z * xv[i].z + xv[i].w * xv[i].w;
+        for (int i = 0; i < R; ++i) {
+            const float4 v = unpack4(xr[i]);
+            ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
 #pragma unroll
@@ -112,11 +143,12 @@ gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __
         for (int i = 0; i < R; ++i) {
             if (r0 + i >= rows) break;
             const float rinv = rsqrtf(fmaf(ss[i], 1.0f / D, eps));
+            const float4 v = unpack4(xr[i]), g = unpack4(zr[i]);
             float4 o;
-            o.x = xv[i].x * (rinv * ws.x) * sigmoid_f(zv[i].x);
-            o.y = xv[i].y * (rinv * ws.y) * sigmoid_f(zv[i].y);
-            o.z = xv[i].z * (rinv * ws.z) * sigmoid_f(zv[i].z);
-            o.w = xv[i].w * (rinv * ws.w) * sigmoid_f(zv[i].w);
+            o.x = v.x * (rinv * ws.x) * sigmoid_f(g.x);
+            o.y = v.y * (rinv * ws.y) * sigmoid_f(g.y);
+            o.z = v.z * (rinv * ws.z) * sigmoid_f(g.z);
+            o.w = v.w * (rinv * ws.w) * sigmoid_f(g.w);
             store4(y + (r0 + i) * D + 4 * lane, o);
         }
     }

@@ -62,9 +62,13 @@ gdn_status launch_gated_rmsnorm(const void* x, const void* z, const float* w, vo
     auto Z = static_cast<const TZ*>(z);
     auto Y = static_cast<TY*>(y);
     if (d == 128 && aligned(x, 16) && aligned(z, 16) && aligned(y, 16) && aligned(w, 16)) {
+        auto kern = gdn::gated_rmsnorm_d128_kernel<TX, TZ, TY>;
+        int per_sm = 0;  // one resident wave, grid-strided
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
         const long long groups = (rows + 3) / 4;  // 4 rows per warp, 8 warps per CTA
-        const unsigned b128 = (unsigned)std::min((groups + 7) / 8, cap);
-        gdn::gated_rmsnorm_d128_kernel<TX, TZ, TY><<<b128, 256, 0, s>>>(X, Z, w, Y, rows, eps);
+        const unsigned b128 = (unsigned)std::min((groups + 7) / 8, (long long)std::max(di.sms, 1) * per_sm);
+        kern<<<b128, 256, 0, s>>>(X, Z, w, Y, rows, eps);
     } else if (d <= 128)
         gdn::gated_rmsnorm_kernel<TX, TZ, TY, 4><<<blocks, 256, 0, s>>>(X, Z, w, Y, rows, d, eps);
     else if (d <= 256)
@@ -113,10 +117,14 @@ gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32
     const int cblocks = (C + 127) / 128;
     if (runs > 0) {
         if (cblocks > 65535) return GDN_ERR_UNSUPPORTED;
-        const long long cap = std::max(1LL, (long long)std::max(di.sms, 1) * 8 / cblocks);  // one wave
+        auto kern = gdn::short_conv_kernel<T, K>;
+        int per_sm = 0;  // one resident wave over all channel blocks
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        const long long cap = std::max(1LL, (long long)std::max(di.sms, 1) * per_sm / cblocks);
         const dim3 grid((unsigned)std::min((runs + 7) / 8, cap), (unsigned)cblocks);
         const long long eq = cu ? 0 : total / N;
-        gdn::short_conv_kernel<T, K><<<grid, 256, 0, s>>>(static_cast<const T*>(x), w, static_cast<T*>(y), cu,
+        kern<<<grid, 256, 0, s>>>(static_cast<const T*>(x), w, static_cast<T*>(y), cu,
                                                            st_in, st_out, N, total, eq, C, ng, eps);
         if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     }

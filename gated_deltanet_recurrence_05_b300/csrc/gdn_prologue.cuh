@@ -16,6 +16,7 @@
 #pragma once
 
 #include "gdn_common.cuh"
+#include "gdn_epilogue.cuh"  // sigmoid_fast
 
 namespace gdn {
 
