@@ -172,6 +172,9 @@ __device__ unsigned long long* g_trace;
 __device__ __forceinline__ void named_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+__device__ __forceinline__ void named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 // Named barrier that also ORs a predicate over its participants, so that a
 // decision to leave a loop is taken by all of them together.
 __device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
@@ -274,9 +277,14 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
         const int lim = isA ? r : (r < min(C, len - n * C) ? r + 1 : 0);
         uint8_t* row = isA ? As + r * 128 : sm + OFF_P + (uint32_t)grp * 8192 + r * 128;
         const bool wide = (wq & 1) != 0;  // rows 32-63
+        // quarters of 16 columns (rows 0-31 need only 0-31); rows 32-63 take
+        // columns 32-63 first: once they are stored, the diagonal blocks 2 and
+        // 3 of A are complete and the warp of P rows 0-31 (done early) solves
+        // them while this warp finishes columns 0-31
 #pragma unroll 1
-        for (int qc = 0; qc < 4; ++qc) {  // quarters of 16 columns (rows 0-31 need only 0-31)
-            if (qc >= 2 && !wide) break;
+        for (int qi = 0; qi < 4; ++qi) {
+            if (qi >= 2 && !wide) break;
+            const int qc = wide ? ((qi + 2) & 3) : qi;
             uint32_t x[16];
             if (qc == 0 && gt == 0) GDN_TRACE_AT(7, n);
             tmem_ld16(tmem + lane_base + T_X + 16 * qc, x);
@@ -312,6 +320,10 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
                 for (int e = 0; e < 16; ++e) dcol[16 * e] = __uint_as_float(x[e]);
             }
             if (qc == 0 && gt == 0) GDN_TRACE_AT(6, n);
+            if (isA && wide && qi == 1) {  // A rows 32-63: diagonal blocks 2, 3 stored
+                __syncwarp();
+                named_arrive(2, 64);
+            }
         }
         if (!isA) fence_async_smem();
     }
@@ -626,12 +638,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_XFREE]);
             if (gt == 0) GDN_TRACE_AT(1, n);
-            named_sync(bar_id, 128);
-            // ---- diagonal blocks T_bb = (I + A_bb)^{-1}, one per warp, by forward
-            //      substitution in fp32 (lane c < 16 solves column c); written to Ts
-            //      (fp16) and, scaled, to the diagonal blocks of Bw and Bu
-            if (lane < 16) {
-                const int b = wq, c = lane;
+            // ---- diagonal blocks T_bb = (I + A_bb)^{-1} by forward substitution
+            //      in fp32, lane c of a half-warp solving column c; written to Ts
+            //      (fp16) and, scaled, to the diagonal blocks of Bw and Bu. The
+            //      warp of A rows 0-31 solves blocks 0, 1 (its own rows) at once;
+            //      the warp of P rows 0-31 solves blocks 2, 3 once the warp of A
+            //      rows 32-63 has stored them (barrier 2)
+            if (wq == 2) named_sync(2, 64);
+            if (wq == 0 || wq == 2) {
+                const int b = (wq == 0 ? 0 : 2) + (lane >> 4), c = lane & 15;
                 // right-looking: once x_ss is final, subtract its column from the rest
                 float xs[16];
 #pragma unroll
