@@ -114,10 +114,12 @@ gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32
                              float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s) {
     const DevInfo di = dev_info();
     const long long runs = (total + 31) / 32;  // 32 tokens per warp
-    const int cblocks = (C + 127) / 128;
+    // 8 channels per lane when the channels and the head size allow it
+    const bool v8 = C % 256 == 0 && (ng == 0 || ng >= 8);
+    const int cblocks = v8 ? C / 256 : (C + 127) / 128;
     if (runs > 0) {
         if (cblocks > 65535) return GDN_ERR_UNSUPPORTED;
-        auto kern = gdn::short_conv_kernel<T, K>;
+        auto kern = v8 ? gdn::short_conv_kernel<T, K, 8> : gdn::short_conv_kernel<T, K, 4>;
         int per_sm = 0;  // one resident wave over all channel blocks
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
             per_sm = 1;

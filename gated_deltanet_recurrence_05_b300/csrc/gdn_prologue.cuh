@@ -42,17 +42,30 @@ __device__ __forceinline__ void store4f(float* p, const float* v) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// silu, then the L2 norm over groups of `ng` channels (ng = 0: none; else a
-// divisor of 128 and a multiple of 4: the group spans ng / 4 lanes)
-__device__ __forceinline__ void silu_norm4(float* s, int ng, float eps) {
+// V consecutive elements (V = 4 or 8) as fp32.
+template <int V, typename T> __device__ __forceinline__ void loadVf(const T* p, float* v) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) s[j] = silu_f(s[j]);
+    for (int h = 0; h < V / 4; ++h) load4f(p + 4 * h, v + 4 * h);
+}
+template <int V, typename T> __device__ __forceinline__ void storeVf(T* p, const float* v) {
+#pragma unroll
+    for (int h = 0; h < V / 4; ++h) store4f(p + 4 * h, v + 4 * h);
+}
+
+// silu, then the L2 norm over groups of `ng` channels (ng = 0: none; else a
+// power of two, at least V, dividing 32 V: the group spans ng / V lanes)
+template <int V>
+__device__ __forceinline__ void silu_norm(float* s, int ng, float eps) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) s[j] = silu_f(s[j]);
     if (ng) {
-        float ss = s[0] * s[0] + s[1] * s[1] + s[2] * s[2] + s[3] * s[3];
-        for (int off = 1; off < ng / 4; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < V; ++j) ss = fmaf(s[j], s[j], ss);
+        for (int off = 1; off < ng / V; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float r = rsqrtf(ss + eps);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[j] *= r;
+        for (int j = 0; j < V; ++j) s[j] *= r;
     }
 }
 
@@ -67,22 +80,23 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int num_seqs, lon
     return lo;
 }
 
-// Each warp filters a run of RUN consecutive tokens for one block of 128
-// channels: the taps slide through registers (one load and one store per
-// token), the weights are loaded once per run, and a run crossing into the
-// next sequence restarts its window from that sequence's state.
-template <typename T, int K>
+// Each warp filters a run of RUN consecutive tokens for one block of 32 V
+// channels (V per lane: 4, or 8 when C and the head size allow): the taps
+// slide through registers (one load and one store per token), the weights are
+// loaded once per run, and a run crossing into the next sequence restarts its
+// window from that sequence's state.
+template <typename T, int K, int V>
 __global__ void __launch_bounds__(256)
 short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
                   const int32_t* __restrict__ cu, const float* __restrict__ st_in, float* __restrict__ st_out,
                   int num_seqs, long long total, long long eq_len, int C, int ng, float eps) {
     constexpr int RUN = 32;
     const int lane = threadIdx.x & 31;
-    const int c = (int)blockIdx.y * 128 + 4 * lane;
-    const bool live = c < C;  // C % 4 == 0: a lane's 4 channels are all in or all out
-    float wv[4][K];
+    const int c = (int)blockIdx.y * (32 * V) + V * lane;
+    const bool live = c < C;  // C % V == 0: a lane's V channels are all in or all out
+    float wv[V][K];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < V; ++j)
 #pragma unroll
         for (int i = 0; i < K; ++i) wv[j][i] = live ? w[(size_t)(c + j) * K + i] : 0.f;
     const long long runs = (total + RUN - 1) / RUN;
@@ -91,7 +105,7 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
         int n = seq_of_token(cu, num_seqs, eq_len, ta);
         long long t0 = cu ? cu[n] : (long long)n * eq_len;
         long long t1 = cu ? cu[n + 1] : t0 + eq_len;
-        float win[K][4];  // win[i] = input at t - (K-1) + i
+        float win[K][V];  // win[i] = input at t - (K-1) + i
         bool bad = false;
         auto restart = [&](long long t) {  // window for token t of sequence n
 #pragma unroll
@@ -99,31 +113,31 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
                 const long long p = t - (K - 1) + i;
                 if (!live) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) win[i][j] = 0.f;
+                    for (int j = 0; j < V; ++j) win[i][j] = 0.f;
                 } else if (p >= t0) {
-                    load4f(x + p * C + c, win[i]);
+                    loadVf<V>(x + p * C + c, win[i]);
                 } else if (st_in) {  // the caller's past: entry p - t0 + K - 1
                     const float* sp = st_in + ((size_t)n * C + c) * (K - 1) + (p - t0 + K - 1);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) win[i][j] = sp[j * (K - 1)];
+                    for (int j = 0; j < V; ++j) win[i][j] = sp[j * (K - 1)];
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) win[i][j] = 0.f;
+                    for (int j = 0; j < V; ++j) win[i][j] = 0.f;
                 }
             }
         };
         if (ta < t0 || ta >= t1 || t0 < 0 || t1 > total) bad = true;
         if (!bad) restart(ta);
         // the run's inputs in batches of 8 tokens, loaded before they are used
-        constexpr int BATCH = 8;
-        float xb[BATCH][4];
+        constexpr int BATCH = V == 4 ? 8 : 4;
+        float xb[BATCH][V];
         for (long long tq = ta; tq < tb && !bad; tq += BATCH) {
 #pragma unroll
             for (int k = 0; k < BATCH; ++k) {
-                if (live && tq + k < tb) load4f(x + (tq + k) * C + c, xb[k]);
+                if (live && tq + k < tb) loadVf<V>(x + (tq + k) * C + c, xb[k]);
                 else {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) xb[k][j] = 0.f;
+                    for (int j = 0; j < V; ++j) xb[k][j] = 0.f;
                 }
             }
 #pragma unroll
@@ -140,30 +154,30 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
                 }
                 if (bad) break;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) win[K - 1][j] = xb[k][j];
-                float acc[4];
+                for (int j = 0; j < V; ++j) win[K - 1][j] = xb[k][j];
+                float acc[V];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < V; ++j) {
                     float a = 0.f;
 #pragma unroll
                     for (int i = 0; i < K; ++i) a = fmaf(wv[j][i], win[i][j], a);
                     acc[j] = a;
                 }
-                silu_norm4(acc, ng, eps);  // every lane takes part in the shuffles
+                silu_norm<V>(acc, ng, eps);  // every lane takes part in the shuffles
                 if (live) {
-                    store4f(y + t * C + c, acc);
+                    storeVf<V>(y + t * C + c, acc);
                     if (st_out && t == t1 - 1) {  // the K-1 newest inputs become the state
                         float* so = st_out + ((size_t)n * C + c) * (K - 1);
 #pragma unroll
                         for (int i = 1; i < K; ++i)
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) so[j * (K - 1) + (i - 1)] = win[i][j];
+                            for (int j = 0; j < V; ++j) so[j * (K - 1) + (i - 1)] = win[i][j];
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < K - 1; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) win[i][j] = win[i + 1][j];
+                    for (int j = 0; j < V; ++j) win[i][j] = win[i + 1][j];
             }
         }
         if (bad && lane == 0) set_device_error(1u);  // cu_seqlens not ascending or out of range
@@ -212,7 +226,7 @@ short_conv_step_kernel(const T* __restrict__ x, const float* __restrict__ w, flo
                 for (int i = 0; i < K - 1; ++i) sp[j * (K - 1) + i] = s[i + 1];
             }
         }
-        silu_norm4(acc, ng, eps);
+        silu_norm<4>(acc, ng, eps);
         if (live) store4f(y + (size_t)n * C + c, acc);
     }
 }
