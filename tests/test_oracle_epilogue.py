@@ -31,12 +31,15 @@ def _rows(n=5, d=16, seed=0, scale=1.0):
 # ----------------------------------------------------------------------------
 
 def pin_hand_example(fn):
-    """o = (3, 4), w = (0, 1), z = (0, ln 3), eps = 0, worked by hand:
-    mean(o^2) = (9 + 16) / 2 = 12.5, sqrt(12.5) = 3.5355339059;
-    y0 = 3 / 3.5355339059 * 1 * 1/2 = 0.4242640687
-    y1 = 4 / 3.5355339059 * 2 * 3/4 = 1.6970562748   (sigmoid(ln 3) = 3/4)."""
-    y = fn(np.array([3.0, 4.0]), np.array([0.0, math.log(3.0)]), np.array([0.0, 1.0]), 0.0)
-    np.testing.assert_allclose(y, [0.4242640687, 1.6970562748], rtol=0, atol=1e-9)
+    """One row worked by hand (tests/golden/gated_rmsnorm_hand_example.json):
+    o = (3, 4), w = (0, 1), z = (0, ln 3), eps = 0 -> (0.4242640687, 1.6970562748)."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                           "gated_rmsnorm_hand_example.json")) as f:
+        G = json.load(f)
+    y = fn(np.array(G["o"]), np.array(G["z"]), np.array(G["w"]), G["eps"])
+    np.testing.assert_allclose(y, G["y"], rtol=0, atol=G["atol"])
 
 
 def pin_unit_rms(fn):

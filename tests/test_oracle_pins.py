@@ -53,33 +53,28 @@ def _rand_problem(total=29, h_qk=2, h_v=4, d_k=6, d_v=5, lengths=None, h0=True, 
 # pins, each taking an oracle object (the real one, or a planted-mistake copy)
 # ----------------------------------------------------------------------------
 
-def pin_hand_example(orc):
-    """d_k=2, d_v=3, three tokens, worked by hand from the rule (scale = 1).
+def _golden(name):
+    import json
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)) as f:
+        return json.load(f)
 
-    S0 = [[1, 2, -1], [0, 1, 3]]
-    t1: k=(1,0), q=(0,1), v=(3,5,1), a=1/2, b=1/2
-        a S0 = [[.5,1,-.5],[0,.5,1.5]]; read (aS0)^T k = (.5,1,-.5)
-        error = v - read = (2.5,4,1.5); S1 = aS0 + k (b error)^T
-        S1 = [[1.75,3,.25],[0,.5,1.5]];  o1 = S1^T q = (0,.5,1.5)
-    t2: k=(.6,.8), q=(1,0), v=(1,-1,2), a=1, b=1
-        read S1^T k = (1.05,2.2,1.35); error = (-.05,-3.2,.65)
-        S2 = [[1.72,1.08,.64],[-.04,-2.06,2.02]];  o2 = (1.72,1.08,.64)
-    t3: same key (.6,.8), q=(.6,.8), v=(2,0,-2), a=1, b=1
-        read S2^T k = (1,-1,2) (the note written at t2); error = (1,1,-4)
-        S3 = [[2.32,1.68,-1.76],[.76,-1.26,-1.18]];  o3 = S3^T k = (2,0,-2)
-    """
-    q = np.array([[[0, 1]], [[1, 0]], [[.6, .8]]], dtype=np.float32)
-    k = np.array([[[1, 0]], [[.6, .8]], [[.6, .8]]], dtype=np.float32)
-    v = np.array([[[3, 5, 1]], [[1, -1, 2]], [[2, 0, -2]]], dtype=np.float32)
-    g = np.array([[math.log(0.5)], [0.0], [0.0]], dtype=np.float32)
-    b = np.array([[0.5], [1.0], [1.0]], dtype=np.float32)
-    S0 = np.array([[[[1, 2, -1], [0, 1, 3]]]], dtype=np.float32)
-    o_exp = np.array([[0, .5, 1.5], [1.72, 1.08, .64], [2, 0, -2]])
-    S_exp = np.array([[2.32, 1.68, -1.76], [.76, -1.26, -1.18]])
+
+def pin_hand_example(orc):
+    """d_k=2, d_v=3, three tokens worked by hand from the rule (scale = 1); the
+    inputs, the derivation and the expected values are in
+    tests/golden/gdn_rule_hand_example.json."""
+    G = _golden("gdn_rule_hand_example.json")
+    q = np.array(G["q"], dtype=np.float32)[:, None, :]
+    k = np.array(G["k"], dtype=np.float32)[:, None, :]
+    v = np.array(G["v"], dtype=np.float32)[:, None, :]
+    g = np.log(np.array(G["alpha"], dtype=np.float64)).astype(np.float32)[:, None]
+    b = np.array(G["beta"], dtype=np.float32)[:, None]
+    S0 = np.array(G["S0"], dtype=np.float32)[None, None]
+    o_exp, S_exp = np.array(G["o"]), np.array(G["S_final"])
     for fn in (orc.recurrent, lambda *a, **kw: orc.chunked(*a, chunk=2, **kw)):
         o, S = fn(q, k, v, g, b, h0=S0, scale=1.0)
-        np.testing.assert_allclose(o[:, 0, :], o_exp, atol=2e-6)
-        np.testing.assert_allclose(S[0, 0], S_exp, atol=2e-6)
+        np.testing.assert_allclose(o[:, 0, :], o_exp, atol=G["atol"])
+        np.testing.assert_allclose(S[0, 0], S_exp, atol=G["atol"])
 
 
 def pin_literal_matrix_form(orc):

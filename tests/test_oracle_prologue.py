@@ -25,12 +25,17 @@ def _x(T, C, seed):
 # pins take (conv, step) callables with the oracle's signatures
 
 def pin_hand_example(conv, step):
-    """K = 3, w = (0.5, -1, 2), x = (1, 2, 3), no activation, by hand:
-    u0 = 2*1 = 2; u1 = -1*1 + 2*2 = 3; u2 = 0.5*1 - 1*2 + 2*3 = 4.5;
-    final state (1 channel, K-1 = 2 entries) = (2, 3)."""
-    y, st = conv(np.array([[1.0], [2.0], [3.0]]), np.array([[0.5, -1.0, 2.0]]), None, None, None, 0)
-    np.testing.assert_allclose(y[:, 0], [2.0, 3.0, 4.5], rtol=0, atol=1e-15)
-    np.testing.assert_allclose(st[0, 0], [2.0, 3.0], rtol=0, atol=0)
+    """One channel worked by hand (tests/golden/short_conv_hand_example.json):
+    K = 3, w = (0.5, -1, 2), x = (1, 2, 3), no activation -> u = (2, 3, 4.5),
+    final state (2, 3)."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                           "short_conv_hand_example.json")) as f:
+        G = json.load(f)
+    y, st = conv(np.array(G["x"])[:, None], np.array([G["w"]]), None, None, None, 0)
+    np.testing.assert_allclose(y[:, 0], G["u"], rtol=0, atol=G["atol"])
+    np.testing.assert_allclose(st[0, 0], G["state_final"], rtol=0, atol=0)
 
 
 def pin_silu_values(conv, step):
