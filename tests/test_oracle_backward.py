@@ -16,7 +16,9 @@ reverse recurrence the oracle uses. The pins are:
     (S_t = e^{G_t} S_0), for every gradient;
   - two homogeneity identities: o is linear in q token by token, so
     <dq, q> = <dO, O>; (O, S_T) is jointly linear in (v, S_0), so
-    <dv, v> + <dS_0, S_0> = <dO, O> + <dS_T, S_T>.
+    <dv, v> + <dS_0, S_0> = <dO, O> + <dS_T, S_T>;
+  - the decay-gradient identity dg_t = <dS_T, S_T> + sum_{r >= t}
+    (<dO_r, o_r> - <dv_r, v_r>), exact for this rule.
 
 ``test_planted_mistakes`` edits the oracle's source (a dropped term, a wrong
 sign, a missing decay, a wrong index, a missing group sum, ...) and checks
@@ -192,8 +194,26 @@ def pin_homogeneity(fn):
     np.testing.assert_allclose(lhs, lo + ls, rtol=1e-11)
 
 
+def pin_decay_gradient_identity(fn):
+    """With D_t = dL/dS_t and S_t - b_t k_t v_t^T = a_t (I - b_t k_t k_t^T) S_{t-1},
+    the rule gives dg_t = <D_t, S_t> - <dv_t, v_t> and <D_{t-1}, S_{t-1}> =
+    dg_t + <dO_{t-1}, o_{t-1}>; unrolled from <D_T, S_T> = <dS_T, S_T> + <dO_T, o_T>:
+        dg_t = <dS_T, S_T> + sum_{r >= t} (<dO_r, o_r> - <dv_r, v_r>)
+    which ties dg to dv and the forward oracle's outputs (per pair)."""
+    P = _problem(6, lens=(11, 6), h_qk=1, h_v=2, d_k=5, d_v=4)
+    got = _call(fn, P)
+    o, S = oracle.recurrent(P["q"], P["k"], P["v"], P["g"], P["beta"], h0=P["h0"], cu_seqlens=P["cu"])
+    cu = P["cu"]
+    for n in range(2):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        for h in range(2):
+            per = np.sum(P["do"][t0:t1, h] * o[t0:t1, h], -1) - np.sum(got["dv"][t0:t1, h] * P["v"][t0:t1, h], -1)
+            ref = float(np.sum(P["dht"][n, h] * S[n, h])) + np.cumsum(per[::-1])[::-1]
+            np.testing.assert_allclose(got["dg"][t0:t1, h], ref, rtol=1e-11, atol=1e-12)
+
+
 PINS = [pin_finite_differences_varlen_gqa, pin_finite_differences_plain, pin_hand_example,
-        pin_beta_zero_closed_form, pin_homogeneity]
+        pin_beta_zero_closed_form, pin_homogeneity, pin_decay_gradient_identity]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
