@@ -6,7 +6,9 @@ workload: B=4 sequences x T=4096 tokens, H_qk=16, H_v=32, d_k=d_v=128, bf16
 q/k/v, fp32 g/beta and state, chunk 64, zero initial state, bf16 output plus
 fp32 final states. value = tokens/s over all ranks. The same JSON line also
 carries the decode step (256 sequences x 32 heads x 128x128 fp32 states,
-1000 consecutive in-place steps, bf16 token inputs) in GB/s.
+1000 consecutive in-place steps, bf16 token inputs) in GB/s, the output
+epilogue and input prologue in GB/s, and the gradient of the prefill
+workload (gdn_chunk_bwd) in tokens/s against the fp32 CUDA-core peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -309,6 +311,7 @@ def run_ours(args, world, rank, local):
     decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
     epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o)
     prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
+    backward = None if args.skip_backward else run_backward(args, dev, peaks, world, w, dd)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -326,6 +329,7 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2 (126 MB) every step; no flush"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
         "clocks": clk.summary(), "decode": decode, "epilogue": epilogue, "prologue": prologue,
+        "backward": backward,
     }
 
 
@@ -479,6 +483,79 @@ def run_prologue(args, dev, peaks, world, w):
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
 
 
+def backward_algorithmic(T, h_v, d_k, d_v):
+    """FLOPs of the gradient by the reverse-order chain rule with the states at
+    hand, per token and value head: the forward quantities it needs (S^T k,
+    the rank-1 state update, S dO) and the reverse step (D += q dO^T, D^T k,
+    D e, S de, D <- a (D - k de^T)): eight passes of one multiply-add per state
+    element, 16 d_k d_v FLOPs."""
+    return 16.0 * d_k * d_v * T * h_v
+
+
+# fp32 CUDA-core peak of the B300: 148 SMs x 128 fp32 lanes x 2 FLOP per FMA x 2032 MHz
+SIMT_FP32_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def run_backward(args, dev, peaks, world, w, dd):
+    """The gradient (gdn_chunk_bwd) of the prefill workload: bf16 dO ~ N(0,1),
+    dS_T ~ N(0, 0.05), workspace allocated once outside the timed region."""
+    import gated_deltanet_recurrence_05_b300 as gdn
+    lengths = w["lengths"]
+    N, T = len(lengths), sum(lengths)
+    h_qk, h_v, d_k, d_v = w["h_qk"], w["h_v"], w["d_k"], w["d_v"]
+    gr = gdn_inputs.make_grads(w, dtype="bf16", dht_std=0.05, seed=args.seed)
+    do, dht = gr["do"].to(dev), gr["dht"].to(dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = (torch.empty(T, h_qk, d_k, **f32), torch.empty(T, h_qk, d_k, **f32), torch.empty(T, h_v, d_v, **f32),
+            torch.empty(T, h_v, **f32), torch.empty(T, h_v, **f32), torch.empty(N, h_v, d_k, d_v, **f32))
+    ws = torch.empty(gdn.chunk_bwd_workspace_size(N, T, h_qk, h_v, d_k, d_v), dtype=torch.uint8, device=dev)
+    cu = dd["cu_seqlens"]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.chunk_bwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], do, dd["h0"], dht, cu,
+                      num_seqs=None if cu is not None else N, out=outs, workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    reps = max(3, min(args.steps, 10))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(reps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if gdn.get_device_error() != 0:
+        raise RuntimeError("device error in the backward")
+    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+    flops = backward_algorithmic(T, h_v, d_k, d_v)
+    tfs = flops / (us / 1e6) / 1e12
+
+    cpu = None
+    if world == 1 and not args.skip_cpu_baseline:
+        from threadpoolctl import threadpool_limits
+        import oracle
+        n_tok = min(512, lengths[0])
+        sl = slice(0, n_tok)
+        with threadpool_limits(1):
+            t0 = time.perf_counter()
+            oracle.recurrent_backward(w["q"][sl, :1], w["k"][sl, :1], w["v"][sl, :1], w["g"][sl, :1],
+                                      w["beta"][sl, :1], gr["do"][sl, :1])
+            sec = time.perf_counter() - t0
+        cpu = {"value": n_tok / sec / h_v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_tok} tokens of one (sequence, value head) pair, scaled to all {h_v} value heads"}
+    return {"workload": f"gradient of the prefill workload (B={N}, T={T // N}, H_qk={h_qk}, H_v={h_v}, "
+                        f"d=128, bf16 q/k/v/dO, fp32 g/beta/dS_T, fp32 gradients)",
+            "us_per_step": us, "tokens_per_s": T * world / (us / 1e6),
+            "gpu_launches": reps * (2 if h_v > h_qk else 1), "cpu_baseline": cpu,
+            "roofline": {"bound": "alu", "achieved": round(tfs, 2), "peak": round(SIMT_FP32_TFLOPS, 1),
+                         "unit": "TFLOP/s", "frac": round(tfs / SIMT_FP32_TFLOPS, 4),
+                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz",
+                         "algorithmic_flops_per_launch": flops}}
+
+
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores (bounded sample)."""
     if rank != 0:
@@ -519,6 +596,7 @@ def main(argv=None):
     ap.add_argument("--skip-decode", action="store_true")
     ap.add_argument("--skip-epilogue", action="store_true", help="skip the epilogue and prologue lines")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-backward", action="store_true", help="skip the gradient line")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)

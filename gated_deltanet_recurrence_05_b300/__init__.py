@@ -65,6 +65,11 @@ def lib():
         L.gdn_short_conv.restype = ctypes.c_int
         L.gdn_short_conv_step.argtypes = [P, P, P, P, I32, I32, I32, I32, F, I32, P]
         L.gdn_short_conv_step.restype = ctypes.c_int
+        L.gdn_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32,
+                                    I32, I32, I32, I32, F, P, ctypes.c_size_t, P]
+        L.gdn_chunk_bwd.restype = ctypes.c_int
+        L.gdn_chunk_bwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32]
+        L.gdn_chunk_bwd_workspace_size.restype = ctypes.c_size_t
         L.gdn_plan_seq_order.argtypes = [P, I32, P]
         L.gdn_plan_seq_order.restype = ctypes.c_int
         L.gdn_get_device_error.argtypes = [P, P]
@@ -149,6 +154,70 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
                              FLAG_FORCE_SIMT if force_simt else 0, _stream(stream))
     _check("gdn_chunk_fwd", st)
     return o, fs
+
+
+def chunk_bwd_workspace_size(num_seqs: int, total_tokens: int, h_qk: int, h_v: int, d_k: int = 128,
+                             d_v: int = 128) -> int:
+    """Bytes of device workspace ``chunk_bwd`` needs for these sizes."""
+    return int(lib().gdn_chunk_bwd_workspace_size(int(num_seqs), int(total_tokens), int(h_qk), int(h_v),
+                                                  int(d_k), int(d_v)))
+
+
+def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+              d_o: torch.Tensor, initial_state: Optional[torch.Tensor] = None,
+              d_final_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None, *,
+              num_seqs: Optional[int] = None, seq_order: Optional[torch.Tensor] = None, scale: float = 0.0,
+              need_d_initial_state: bool = True, workspace: Optional[torch.Tensor] = None, out=None,
+              stream=None):
+    """Gradient of the recurrence (see include/gdn.h, gdn_chunk_bwd).
+
+    Forward inputs as for ``chunk_fwd``; d_o: [T, H_v, d_v] (fp32 or bf16);
+    d_final_state: [N, H_v, d_k, d_v] fp32 or None. ``workspace`` is a CUDA
+    uint8 tensor of at least ``chunk_bwd_workspace_size`` bytes (allocated
+    here when None). ``out`` may give the six output tensors. Returns
+    (dq, dk, dv, dg, dbeta, d_initial_state or None), all fp32.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("d_o", d_o)):
+        _dev(t, name)
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    if cu_seqlens is not None:
+        _dev(cu_seqlens, "cu_seqlens")
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    for name, t in (("seq_order", seq_order), ("initial_state", initial_state),
+                    ("d_final_state", d_final_state)):
+        if t is not None:
+            _dev(t, name)
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dev = v.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    if out is not None:
+        dq, dk, dv, dg, db, dh0 = out
+    else:
+        dq = torch.empty((T, h_qk, d_k), **f32)
+        dk = torch.empty((T, h_qk, d_k), **f32)
+        dv = torch.empty((T, h_v, d_v), **f32)
+        dg = torch.empty((T, h_v), **f32)
+        db = torch.empty((T, h_v), **f32)
+        dh0 = torch.empty((N, h_v, d_k, d_v), **f32) if need_d_initial_state else None
+    need = chunk_bwd_workspace_size(N, T, h_qk, h_v, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace")
+    st = lib().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                             _ptr(cu_seqlens), _ptr(seq_order), _ptr(d_o), _ptr(d_final_state), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), N, T, h_qk, h_v, d_k, d_v,
+                             _code(q), _code(d_o), float(scale), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("gdn_chunk_bwd", st)
+    return dq, dk, dv, dg, db, dh0
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

@@ -15,6 +15,7 @@
 #include "gdn_decode.cuh"
 #include "gdn_chunk_simt.cuh"
 #include "gdn_chunk_tc.cuh"
+#include "gdn_backward.cuh"
 
 namespace {
 
@@ -176,7 +177,53 @@ bool ok_norm_group(int ng, int C) {
     return ng == 0 || ((ng == 4 || ng == 8 || ng == 16 || ng == 32 || ng == 64 || ng == 128) && C % ng == 0);
 }
 
+// Workspace layout of gdn_chunk_bwd: checkpoints, then (grouped heads only)
+// the per-value-head dq and dk parts, each part 256-byte aligned.
+struct BwdLayout { long long nslots = 0; size_t ckpt = 0, part = 0, total = 0; };
+BwdLayout bwd_layout(int32_t N, int64_t T, int32_t h_qk, int32_t h_v) {
+    BwdLayout L;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    L.nslots = T / gdn::bwd::BLK + N + 1;
+    L.ckpt = up((size_t)h_v * (size_t)L.nslots * gdn::bwd::SD * sizeof(float));
+    L.part = h_v > h_qk ? up((size_t)T * h_v * gdn::bwd::D * sizeof(float)) : 0;
+    L.total = L.ckpt + 2 * L.part;
+    return L;
+}
+
+bool bwd_sizes_ok(int32_t N, int64_t T, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v) {
+    return N >= 0 && T >= 0 && h_qk > 0 && h_v > 0 && h_v % h_qk == 0 && d_k > 0 && d_v > 0;
+}
+
+template <typename TIn, typename TdO>
+gdn_status launch_bwd(gdn::bwd::Args a, float* dq, float* dk, char* ws, const BwdLayout& L, cudaStream_t s) {
+    const long long blocks = (long long)a.num_seqs * a.h_v;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const DevInfo di = dev_info();
+    if (di.smem_optin < (int)gdn::bwd::SMEM_BYTES) return di.smem_optin <= 0 ? GDN_ERR_CUDA : GDN_ERR_UNSUPPORTED;
+    auto kern = gdn::bwd::backward_kernel<TIn, TdO>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gdn::bwd::SMEM_BYTES) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    a.ckpt = reinterpret_cast<float*>(ws);
+    a.nslots = L.nslots;
+    float* dq_part = L.part ? reinterpret_cast<float*>(ws + L.ckpt) : dq;
+    float* dk_part = L.part ? reinterpret_cast<float*>(ws + L.ckpt + L.part) : dk;
+    a.dq = dq_part;
+    a.dk = dk_part;
+    kern<<<(unsigned)blocks, gdn::bwd::NT, gdn::bwd::SMEM_BYTES, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    if (L.part && a.total > 0) {
+        const long long units = a.total * a.h_qk * (gdn::bwd::D / 4);
+        const long long cap = (long long)std::max(di.sms, 1) * 8;
+        const unsigned grid = (unsigned)std::min(cap, (units + 255) / 256);
+        gdn::bwd::group_sum_kernel<<<grid, 256, 0, s>>>(dq_part, dk_part, dq, dk, units, a.h_qk, a.grp);
+        if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
+
 
 extern "C" {
 
@@ -191,7 +238,7 @@ const char* gdn_status_string(gdn_status s) {
     return "GDN_ERR_UNKNOWN";
 }
 
-int32_t gdn_version(void) { return 101; }
+int32_t gdn_version(void) { return 102; }
 
 gdn_status gdn_plan_seq_order(const int32_t* cu, int32_t num_seqs, int32_t* order_out) {
     if (num_seqs < 0 || (num_seqs > 0 && (cu == nullptr || order_out == nullptr))) return GDN_ERR_INVALID_ARG;
@@ -371,6 +418,50 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     if (bf_in) return launch_simt<__nv_bfloat16, float>(a, smem, s);
     if (bf_out) return launch_simt<float, __nv_bfloat16>(a, smem, s);
     return launch_simt<float, float>(a, smem, s);
+}
+
+size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v,
+                                    int32_t d_k, int32_t d_v) {
+    if (!bwd_sizes_ok(num_seqs, total_tokens, h_qk, h_v, d_k, d_v) || total_tokens > 0x7fffffffLL) return 0;
+    return bwd_layout(num_seqs, total_tokens, h_qk, h_v).total;
+}
+
+gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens, const int32_t* seq_order,
+                         const void* d_o, const float* d_final_state, float* dq, float* dk, float* dv,
+                         float* dg, float* dbeta, float* d_initial_state, int32_t num_seqs,
+                         int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                         int32_t dtype_qkv, int32_t dtype_do, float scale, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+    if (!bwd_sizes_ok(num_seqs, total_tokens, h_qk, h_v, d_k, d_v)) return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_do)) return GDN_ERR_INVALID_ARG;
+    if (d_k != gdn::bwd::D || d_v != gdn::bwd::D) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
+    if (total_tokens > 0 &&
+        (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) || !ok_ptr(d_o) ||
+         !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv) || !ok_ptr(dg, 4) || !ok_ptr(dbeta, 4)))
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_opt(initial_state) || !ok_opt(d_final_state) || !ok_opt(d_initial_state) || !ok_opt(cu_seqlens, 4) ||
+        !ok_opt(seq_order, 4))
+        return GDN_ERR_INVALID_ARG;
+    const BwdLayout L = bwd_layout(num_seqs, total_tokens, h_qk, h_v);
+    if (!ok_ptr(workspace, 256) || workspace_bytes < L.total) return GDN_ERR_INVALID_ARG;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
+    gdn::bwd::Args a{};
+    a.q = q; a.k = k; a.v = v; a.dout = d_o; a.g = g; a.beta = beta;
+    a.h0 = initial_state; a.dht = d_final_state; a.cu = cu_seqlens; a.order = seq_order;
+    a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = d_initial_state;
+    a.total = total_tokens; a.eq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
+    a.num_seqs = num_seqs; a.h_qk = h_qk; a.h_v = h_v; a.grp = h_v / h_qk; a.scale = scale;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    const bool bq = dtype_qkv == GDN_BF16, bd = dtype_do == GDN_BF16;
+    if (bq && bd) return launch_bwd<__nv_bfloat16, __nv_bfloat16>(a, dq, dk, ws, L, s);
+    if (bq) return launch_bwd<__nv_bfloat16, float>(a, dq, dk, ws, L, s);
+    if (bd) return launch_bwd<float, __nv_bfloat16>(a, dq, dk, ws, L, s);
+    return launch_bwd<float, float>(a, dq, dk, ws, L, s);
 }
 
 #ifdef GDN_TRACE

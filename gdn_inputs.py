@@ -21,7 +21,9 @@ alpha = exp(g), initial states N(0, 0.02) where one is given):
 
 Draw order (fixed, one ``torch.Generator`` seeded with ``seed``): sequence
 lengths (varlen only) -> q -> k -> v -> beta-raw -> g-raw -> h0. Every value is
-drawn in fp32 and then cast to the storage dtype.
+drawn in fp32 and then cast to the storage dtype. The incoming gradients of a
+backward problem (``make_grads``) come from a second generator, so drawing
+them leaves the forward inputs unchanged.
 
 Layouts (dense, row-major):
   q, k : [T_total, H_qk, d_k]      v : [T_total, H_v, d_v]
@@ -35,7 +37,7 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_workload"]
+__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_workload", "make_grads"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -165,3 +167,18 @@ def make_workload(name: str, seed: int = 0, steps: Optional[int] = None) -> dict
     return make_prefill(h_qk=w.h_qk, h_v=w.h_v, d_k=w.d_k, d_v=w.d_v, dtype=w.dtype,
                         batch=w.batch, seqlen=w.seqlen, g_shift=w.g_shift,
                         h0_std=w.h0_std, seed=seed)
+
+
+def make_grads(problem: dict, *, dtype: str = "f32", dht_std: float = 0.0, seed: int = 0) -> dict:
+    """Incoming gradients for a backward problem drawn by ``make_prefill``:
+    dO ~ N(0, 1) shaped like v (stored in ``dtype``) and, when dht_std > 0,
+    dS_T ~ N(0, dht_std) shaped like the states (fp32; None otherwise).
+    Drawn from its own generator seeded with ``seed + 7919``."""
+    gen = _gen(seed + 7919)
+    v = problem["v"]
+    n = len(problem["lengths"])
+    do = torch.randn(v.shape, generator=gen)
+    dht = None
+    if dht_std > 0:
+        dht = torch.randn(n, v.shape[1], problem["q"].shape[2], v.shape[2], generator=gen) * dht_std
+    return dict(do=do.to(_DT[dtype]).contiguous(), dht=dht)

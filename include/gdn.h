@@ -1,5 +1,6 @@
 /*
- * gdn.h -- C ABI of the B300 (sm_103a) Gated DeltaNet forward recurrence.
+ * gdn.h -- C ABI of the B300 (sm_103a) Gated DeltaNet recurrence (forward, decode,
+ *          backward, and the layer's input prologue and output epilogue).
  *
  * The operation (per sequence n and value head h, with the state S of shape
  * d_k x d_v, rows indexed by the key dimension):
@@ -221,6 +222,61 @@ gdn_status gdn_short_conv(const void* x, const float* w, void* y, const int32_t*
 gdn_status gdn_short_conv_step(const void* x, const float* w, float* conv_state, void* y,
                                int32_t num_seqs, int32_t channels, int32_t kernel_size,
                                int32_t norm_group, float eps, int32_t dtype, void* stream);
+
+/*
+ * gdn_chunk_bwd -- gradient of the recurrence (the backward pass of
+ * gdn_chunk_fwd, for training). The pages count the training cost of a design
+ * change next to its prefill and decode cost ("On the Design of Qwen3.8-Next
+ * Architecture", arXiv abstract); the gradient itself is fixed by the rule
+ * above. With L = sum_t <dO_t, o_t> + <dS_T, S_T> it writes
+ *
+ * dq, dk          [T_total, H_qk, d_k] fp32  dL/dq, dL/dk (summed over the value
+ *                 heads that share a q/k head)
+ * dv              [T_total, H_v, d_v]  fp32  dL/dv
+ * dg, dbeta       [T_total, H_v]       fp32  dL/dg (g the log-decay), dL/dbeta
+ * d_initial_state [N, H_v, d_k, d_v]   fp32  dL/dS_0; NULL = not written
+ *
+ * from the forward inputs (q, k, v, g, beta, initial_state, cu_seqlens,
+ * seq_order, scale: exactly as for gdn_chunk_fwd) and
+ *
+ * d_o             [T_total, H_v, d_v]  dtype_do (F32 or BF16)   dL/do
+ * d_final_state   [N, H_v, d_k, d_v]   fp32, NULL = zero         dL/dS_T
+ *
+ * workspace       device scratch of at least gdn_chunk_bwd_workspace_size()
+ *                 bytes, 256-byte aligned, owned by the caller; its contents
+ *                 on entry do not matter and are garbage on return. It holds
+ *                 the state at the start of every block of 32 tokens
+ *                 (64 KB per block and value head) and, when H_v > H_qk,
+ *                 the per-value-head parts of dq and dk.
+ *
+ * All arithmetic is fp32 (bf16 inputs are widened exactly). The kernel
+ * replays the forward from the checkpoints, so o and the final state of the
+ * forward call are not needed. Outputs must not overlap the inputs.
+ * Only d_k = d_v = 128 is compiled (GDN_ERR_UNSUPPORTED otherwise). Other
+ * errors as for gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG for a missing or
+ * too small workspace.
+ */
+gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v,
+                         const float* g, const float* beta,
+                         const float* initial_state, const int32_t* cu_seqlens,
+                         const int32_t* seq_order,
+                         const void* d_o, const float* d_final_state,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                         float* d_initial_state,
+                         int32_t num_seqs, int64_t total_tokens,
+                         int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                         int32_t dtype_qkv, int32_t dtype_do, float scale,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_chunk_bwd_workspace_size -- bytes of workspace gdn_chunk_bwd needs for
+ * these sizes (host only, launches nothing). It depends on N, T_total and
+ * the head counts only, not on cu_seqlens: with blocks of 32 tokens,
+ * H_v * (T_total / 32 + N + 1) states of d_k * d_v fp32, plus
+ * 2 * T_total * H_v * d_k fp32 when H_v > H_qk. Returns 0 for invalid sizes.
+ */
+size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
+                                    int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v);
 
 /*
  * gdn_plan_seq_order -- HOST helper: writes into order_out[0..N-1] (host

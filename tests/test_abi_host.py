@@ -35,7 +35,7 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
-                 "gdn_short_conv", "gdn_short_conv_step",
+                 "gdn_short_conv", "gdn_short_conv_step", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size",
                  "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
         assert need in names
@@ -219,3 +219,50 @@ def test_short_conv_step_host_validation(L):
     assert call(y=FAKE) == INVALID
     assert call(K=5) == UNSUPPORTED
     assert call(N=0) == OK
+
+
+def _bwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, order=None, do=FAKE, dht=None,
+             dq=FAKE, dk=FAKE, dv=FAKE, dg=FAKE, db=FAKE, dh0=None, N=2, T=64, h_qk=2, h_v=4, d_k=128,
+             d_v=128, dtq=1, dtd=1, scale=0.0, ws=FAKE, ws_bytes=None)
+    a.update(kw)
+    if a["ws_bytes"] is None:
+        a["ws_bytes"] = L.gdn_chunk_bwd_workspace_size(a["N"], a["T"], a["h_qk"], a["h_v"], a["d_k"], a["d_v"])
+    return L.gdn_chunk_bwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["cu"], a["order"], a["do"],
+                           a["dht"], a["dq"], a["dk"], a["dv"], a["dg"], a["db"], a["dh0"], a["N"], a["T"],
+                           a["h_qk"], a["h_v"], a["d_k"], a["d_v"], a["dtq"], a["dtd"], a["scale"], a["ws"],
+                           a["ws_bytes"], None)
+
+
+# Every case below has at least one invalid argument, so nothing is launched.
+@pytest.mark.parametrize("kw,status", [
+    (dict(ws_bytes=0), INVALID),                 # workspace too small
+    (dict(ws=None), INVALID),
+    (dict(ws=FAKE + 16), INVALID),               # workspace needs 256 bytes
+    (dict(q=None), INVALID),
+    (dict(do=FAKE + 8), INVALID),
+    (dict(dq=FAKE + 4), INVALID),                # gradients need 16 bytes
+    (dict(dg=FAKE + 2), INVALID),
+    (dict(dh0=FAKE + 8), INVALID),
+    (dict(dht=FAKE + 4), INVALID),
+    (dict(h_qk=3), INVALID),
+    (dict(dtd=2), INVALID),
+    (dict(N=3, T=64), INVALID),                  # equal lengths need T % N == 0
+    (dict(d_k=64, d_v=64), UNSUPPORTED),         # only d = 128 is compiled
+    (dict(d_v=96), UNSUPPORTED),
+    (dict(N=0, T=0), OK),                        # nothing to do
+    (dict(N=0, T=4), INVALID),
+])
+def test_chunk_bwd_host_validation(L, kw, status):
+    assert _bwd(L, **kw) == status
+
+
+def test_chunk_bwd_workspace_size(L):
+    f = L.gdn_chunk_bwd_workspace_size
+    st = 128 * 128 * 4
+    # checkpoints: H_v * (T/32 + N + 1) states; grouped heads add two [T, H_v, 128] fp32 parts
+    assert f(4, 16384, 16, 32, 128, 128) == 32 * (512 + 5) * st + 2 * 16384 * 32 * 128 * 4
+    assert f(1, 100, 4, 4, 128, 128) == 4 * (3 + 2) * st
+    assert f(0, 0, 1, 1, 128, 128) == 1 * st
+    assert f(-1, 0, 1, 1, 128, 128) == 0 and f(1, 10, 3, 4, 128, 128) == 0
+    assert gdn.chunk_bwd_workspace_size(4, 16384, 16, 32) == f(4, 16384, 16, 32, 128, 128)
