@@ -68,6 +68,9 @@ def lib():
         L.gdn_chunk_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32,
                                     I32, I32, I32, I32, F, P, ctypes.c_size_t, P]
         L.gdn_chunk_bwd.restype = ctypes.c_int
+        L.gdn_chunk_bwd_static.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, I32, I64, I32,
+                                           I32, I32, I32, I32, I32, F, P]
+        L.gdn_chunk_bwd_static.restype = ctypes.c_int
         L.gdn_chunk_bwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32]
         L.gdn_chunk_bwd_workspace_size.restype = ctypes.c_size_t
         L.gdn_plan_seq_order.argtypes = [P, I32, P]

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 #include <numeric>
 #include <vector>
 
@@ -224,6 +225,31 @@ gdn_status launch_bwd(gdn::bwd::Args a, float* dq, float* dk, char* ws, const Bw
 
 }  // namespace
 
+
+// Scratch of gdn_chunk_bwd_static: a fixed device array in this module, so
+// that callers without an allocator can still take the gradient. Host code
+// must not use the symbol's name as a pointer; the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) unsigned char g_bwd_static_scratch[GDN_BWD_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kMaxDevices] = {};
+
+gdn_status static_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bwd_static_scratch) != cudaSuccess || p == nullptr) return GDN_ERR_CUDA;
+        g_static_scratch_ptr[dev] = p;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return GDN_OK;
+}
+}  // namespace
 
 extern "C" {
 
@@ -462,6 +488,25 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
     if (bq) return launch_bwd<__nv_bfloat16, float>(a, dq, dk, ws, L, s);
     if (bd) return launch_bwd<float, __nv_bfloat16>(a, dq, dk, ws, L, s);
     return launch_bwd<float, float>(a, dq, dk, ws, L, s);
+}
+
+gdn_status gdn_chunk_bwd_static(const void* q, const void* k, const void* v, const float* g,
+                                const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                                const int32_t* seq_order, const void* d_o, const float* d_final_state, float* dq,
+                                float* dk, float* dv, float* dg, float* dbeta, float* d_initial_state,
+                                int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k,
+                                int32_t d_v, int32_t dtype_qkv, int32_t dtype_do, float scale, void* stream) {
+    // size checks on the host first: nothing touches the device for a rejected call
+    const size_t need = gdn_chunk_bwd_workspace_size(num_seqs, total_tokens, h_qk, h_v, d_k, d_v);
+    if (need == 0) return GDN_ERR_INVALID_ARG;
+    if (d_k != gdn::bwd::D || d_v != gdn::bwd::D) return GDN_ERR_UNSUPPORTED;
+    if (need > GDN_BWD_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    const gdn_status st = static_scratch_address(&scratch);
+    if (st != GDN_OK) return st;
+    return gdn_chunk_bwd(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq, dk, dv, dg,
+                         dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, d_k, d_v, dtype_qkv, dtype_do,
+                         scale, scratch, GDN_BWD_STATIC_SCRATCH_BYTES, stream);
 }
 
 #ifdef GDN_TRACE

@@ -279,6 +279,43 @@ size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
                                     int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v);
 
 /*
+ * gdn_chunk_bwd_static -- gdn_chunk_bwd for callers that cannot allocate
+ * device memory. (The paper has no counterpart: this is a library
+ * convenience.) Some callers have no way to obtain a device buffer for the
+ * workspace at the point where they need the gradient: a host that fixes
+ * its memory budget when it starts and hands out no further allocations, a
+ * plug-in that is given tensors but no allocator, or a code path where a
+ * cudaMalloc (which may synchronise the device) is not allowed. This entry
+ * point takes the same arguments as gdn_chunk_bwd minus the workspace and
+ * uses instead a scratch array built into the library: GDN_BWD_STATIC_SCRATCH_BYTES
+ * (64 MiB) of device memory that every GPU which loads the library reserves
+ * until the process exits. It allocates nothing itself.
+ *
+ * Limit: the problem must satisfy gdn_chunk_bwd_workspace_size(...) <=
+ * GDN_BWD_STATIC_SCRATCH_BYTES (for example one sequence of up to 4096
+ * tokens with 4 value heads and no head sharing: 4 * 133 states of 64 KB);
+ * larger problems return GDN_ERR_UNSUPPORTED before touching the device.
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture. All calls on a device share the one array and it keeps
+ * whatever the last call left there (nothing in it needs to start at zero):
+ * calls whose executions overlap on the GPU (other streams, other threads)
+ * race on it and give wrong results, so serialise them.
+ * Errors otherwise as for gdn_chunk_bwd.
+ */
+#define GDN_BWD_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+gdn_status gdn_chunk_bwd_static(const void* q, const void* k, const void* v,
+                                const float* g, const float* beta,
+                                const float* initial_state, const int32_t* cu_seqlens,
+                                const int32_t* seq_order,
+                                const void* d_o, const float* d_final_state,
+                                float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                                float* d_initial_state,
+                                int32_t num_seqs, int64_t total_tokens,
+                                int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                                int32_t dtype_qkv, int32_t dtype_do, float scale, void* stream);
+
+/*
  * gdn_plan_seq_order -- HOST helper: writes into order_out[0..N-1] (host
  * memory) the sequence indices sorted by length, longest first (ties keep
  * index order), from a HOST copy of cu_seqlens [N + 1]. The caller copies the
