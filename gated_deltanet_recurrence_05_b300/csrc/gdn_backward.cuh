@@ -23,13 +23,14 @@
 // q_t . dq_t = dO_t . o_t), so no inner product with a whole state is needed.
 //
 // Design (one CTA of 256 threads per (sequence, value head), d_k = d_v = 128):
-//  * Phase 1 runs the recurrence forward in fp32 registers and stores the
+//  * Phase 1 runs the recurrence forward in fp32 registers. It stores the
 //    state at the start of every block of BLK = 32 tokens (the checkpoints,
-//    64 KB each, in the caller's workspace).
+//    64 KB each) and, per token, the error e_t and q_t . dq_t in the caller's
+//    workspace, and writes dq_t = scale S_t dO_t (it holds S_t).
 //  * Phase 2 walks the blocks last to first. For a block it stages the
-//    block's q, k, v, dO, g, beta in shared memory, replays the block forward
-//    from its checkpoint (producing e_t and dq_t, which needs S_t), reloads the
-//    checkpoint S_b and runs the reverse steps with D in registers.
+//    block's q, k, v, dO, g, beta and the stored e_t in shared memory, loads
+//    the block's checkpoint S_b and runs the reverse steps with D in
+//    registers.
 //  * S_{t-1} is never stored per token: inside a block
 //      S_{t-1} = gam_{t-1} S_b + sum_{s<t} Gam_{t-1,s} b_s k_s e_s^T
 //    (gam, Gam: products of the block's decays), so the one state product of
@@ -74,7 +75,8 @@ constexpr int OFF_L = OFF_B + BLK;
 constexpr int OFF_QDQ = OFF_L + BLK;
 constexpr int OFF_VDV = OFF_QDQ + BLK * NW;
 constexpr int OFF_DB = OFF_VDV + BLK * NW;
-constexpr int OFF_MISC = OFF_DB + BLK * NW;
+constexpr int OFF_QT = OFF_DB + BLK * NW;        // q_t . dq_t of the block's tokens
+constexpr int OFF_MISC = OFF_QT + BLK;
 constexpr int SMEM_FLOATS = OFF_MISC + 16;
 constexpr size_t SMEM_BYTES = (size_t)SMEM_FLOATS * sizeof(float);
 static_assert(OFF_RED % 4 == 0 && RED % 4 == 0, "float4 column-sum stores");
@@ -86,6 +88,8 @@ struct Args {
     float* dq; float* dk;          // [T, H_v, 128]: final when H_v == H_qk, else per value head
     float* dv; float* dg; float* dbeta; float* dh0;
     float* ckpt;                   // [H_v, nslots, 128, 128]
+    float* e_ws;                   // [T, H_v, 128]: e_t of every token (phase 1 -> phase 2)
+    float* qdq_ws;                 // [T, H_v]: q_t . dq_t
     long long nslots;
     long long total, eq_len;
     int num_seqs, h_qk, h_v, grp;
@@ -140,7 +144,7 @@ __device__ __forceinline__ void zero_state(float (&S)[16][4]) {
 
 // Stage tokens [tb0, tb0 + n) of the sequence into shared memory as fp32
 // (rows j >= n are zero, g = beta = 0), and the running sum of g in the block.
-template <typename TIn, typename TdO, bool WITH_QDO>
+template <typename TIn, typename TdO>
 __device__ __forceinline__ void load_block(float* sm, const Args& p, long long tb0, int n, int h, int hk) {
     const TIn* q = static_cast<const TIn*>(p.q);
     const TIn* k = static_cast<const TIn*>(p.k);
@@ -155,17 +159,13 @@ __device__ __forceinline__ void load_block(float* sm, const Args& p, long long t
             const size_t v_off = ((size_t)t * p.h_v + h) * D + c;
             kk = load4(k + qk_off);
             kv = load4(v + v_off);
-            if (WITH_QDO) {
-                kq = load4(q + qk_off);
-                kd = load4(dO + v_off);
-            }
+            kq = load4(q + qk_off);
+            kd = load4(dO + v_off);
         }
         *reinterpret_cast<float4*>(sm + OFF_K + j * D + c) = kk;
         *reinterpret_cast<float4*>(sm + OFF_V + j * D + c) = kv;
-        if (WITH_QDO) {
-            *reinterpret_cast<float4*>(sm + OFF_Q + j * D + c) = kq;
-            *reinterpret_cast<float4*>(sm + OFF_DO + j * D + c) = kd;
-        }
+        *reinterpret_cast<float4*>(sm + OFF_Q + j * D + c) = kq;
+        *reinterpret_cast<float4*>(sm + OFF_DO + j * D + c) = kd;
     }
     if (threadIdx.x < 32) {
         const int j = threadIdx.x;
@@ -203,9 +203,8 @@ __device__ __forceinline__ float column_sum(float* sm, const float (&c)[4], int 
 }
 
 // One forward token j of the staged block: S <- a S + b k e^T with
-// e = v - a S^T k stored to shared memory. WITH_DQ also forms dq = scale S dO
-// from the new state (written to p.dq) and the per-warp parts of q . dq.
-template <bool WITH_DQ>
+// e = v - a S^T k stored to shared memory; then dq = scale S dO from the new
+// state (written to p.dq) and the per-warp parts of q . dq.
 __device__ __forceinline__ void forward_token(float* sm, float (&S)[16][4], const Args& p, int j,
                                               long long t, int h, int warp, int lane, int r0, int c0) {
     float kr[16];
@@ -228,13 +227,6 @@ __device__ __forceinline__ void forward_token(float* sm, float (&S)[16][4], cons
     __syncthreads();
     const float4 e4 = *reinterpret_cast<const float4*>(sm + OFF_E + j * D + c0);
     const float u[4] = {b * e4.x, b * e4.y, b * e4.z, b * e4.w};
-    if (!WITH_DQ) {
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) S[r][cc] = fmaf(a, S[r][cc], kr[r] * u[cc]);
-        return;
-    }
     const float4 d4 = *reinterpret_cast<const float4*>(sm + OFF_DO + j * D + c0);
     const float dov[4] = {d4.x, d4.y, d4.z, d4.w};
     float rr[16];
@@ -355,9 +347,10 @@ __device__ __forceinline__ void finish_block(float* sm, const Args& p, long long
     if (warp == 0) {
         float x = 0.f, dbv = 0.f;
         if (lane < n) {
+            x = sm[OFF_QT + lane];
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                x += sm[OFF_QDQ + lane * NW + w] - sm[OFF_VDV + lane * NW + w];
+                x -= sm[OFF_VDV + lane * NW + w];
                 dbv += sm[OFF_DB + lane * NW + w];
             }
         }
@@ -405,9 +398,22 @@ __global__ void __launch_bounds__(NT, 1) backward_kernel(const Args p) {
         const int nt = (int)min((long long)BLK, t1 - tb0);
         store_state(S, ck + (size_t)bi * SD, r0, c0);
         __syncthreads();
-        load_block<TIn, TdO, false>(sm, p, tb0, nt, h, hk);
+        load_block<TIn, TdO>(sm, p, tb0, nt, h, hk);
         __syncthreads();
-        for (int j = 0; j < nt; ++j) forward_token<false>(sm, S, p, j, tb0 + j, h, warp, lane, r0, c0);
+        for (int j = 0; j < nt; ++j) forward_token(sm, S, p, j, tb0 + j, h, warp, lane, r0, c0);
+        __syncthreads();
+        // hand e_t and q_t . dq_t of the block to phase 2
+        for (int idx = threadIdx.x; idx < nt * (D / 4); idx += NT) {
+            const int j = idx >> 5, c = (idx & 31) * 4;
+            *reinterpret_cast<float4*>(p.e_ws + ((size_t)(tb0 + j) * p.h_v + h) * D + c) =
+                *reinterpret_cast<const float4*>(sm + OFF_E + j * D + c);
+        }
+        if (warp == 0 && lane < nt) {
+            float x = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) x += sm[OFF_QDQ + lane * NW + w];
+            p.qdq_ws[(size_t)(tb0 + lane) * p.h_v + h] = x;
+        }
     }
     // <dS_T, S_T> starts the decay gradient's running sum
     float carry = 0.f;
@@ -436,10 +442,14 @@ __global__ void __launch_bounds__(NT, 1) backward_kernel(const Args p) {
         const long long tb0 = t0 + (long long)bi * BLK;
         const int nt = (int)min((long long)BLK, t1 - tb0);
         __syncthreads();
-        load_block<TIn, TdO, true>(sm, p, tb0, nt, h, hk);
+        load_block<TIn, TdO>(sm, p, tb0, nt, h, hk);
+        for (int idx = threadIdx.x; idx < nt * (D / 4); idx += NT) {
+            const int j = idx >> 5, c = (idx & 31) * 4;
+            *reinterpret_cast<float4*>(sm + OFF_E + j * D + c) =
+                *reinterpret_cast<const float4*>(p.e_ws + ((size_t)(tb0 + j) * p.h_v + h) * D + c);
+        }
+        if (threadIdx.x < nt) sm[OFF_QT + threadIdx.x] = p.qdq_ws[(size_t)(tb0 + threadIdx.x) * p.h_v + h];
         __syncthreads();
-        load_state(S, ck + (size_t)bi * SD, r0, c0);
-        for (int j = 0; j < nt; ++j) forward_token<true>(sm, S, p, j, tb0 + j, h, warp, lane, r0, c0);
         load_state(S, ck + (size_t)bi * SD, r0, c0);   // S_b for the reverse steps
         for (int j = nt - 1; j >= 0; --j) reverse_token(sm, Dm, S, p, j, tb0 + j, h, warp, lane, r0, c0);
         finish_block(sm, p, tb0, nt, h, warp, lane, carry);

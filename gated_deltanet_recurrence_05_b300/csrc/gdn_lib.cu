@@ -180,14 +180,16 @@ bool ok_norm_group(int ng, int C) {
 
 // Workspace layout of gdn_chunk_bwd: checkpoints, then (grouped heads only)
 // the per-value-head dq and dk parts, each part 256-byte aligned.
-struct BwdLayout { long long nslots = 0; size_t ckpt = 0, part = 0, total = 0; };
+struct BwdLayout { long long nslots = 0; size_t ckpt = 0, part = 0, e = 0, qdq = 0, total = 0; };
 BwdLayout bwd_layout(int32_t N, int64_t T, int32_t h_qk, int32_t h_v) {
     BwdLayout L;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     L.nslots = T / gdn::bwd::BLK + N + 1;
     L.ckpt = up((size_t)h_v * (size_t)L.nslots * gdn::bwd::SD * sizeof(float));
     L.part = h_v > h_qk ? up((size_t)T * h_v * gdn::bwd::D * sizeof(float)) : 0;
-    L.total = L.ckpt + 2 * L.part;
+    L.e = up((size_t)T * h_v * gdn::bwd::D * sizeof(float));
+    L.qdq = up((size_t)T * h_v * sizeof(float));
+    L.total = L.ckpt + 2 * L.part + L.e + L.qdq;
     return L;
 }
 
@@ -211,6 +213,8 @@ gdn_status launch_bwd(gdn::bwd::Args a, float* dq, float* dk, char* ws, const Bw
     float* dk_part = L.part ? reinterpret_cast<float*>(ws + L.ckpt + L.part) : dk;
     a.dq = dq_part;
     a.dk = dk_part;
+    a.e_ws = reinterpret_cast<float*>(ws + L.ckpt + 2 * L.part);
+    a.qdq_ws = reinterpret_cast<float*>(ws + L.ckpt + 2 * L.part + L.e);
     kern<<<(unsigned)blocks, gdn::bwd::NT, gdn::bwd::SMEM_BYTES, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
     if (L.part && a.total > 0) {

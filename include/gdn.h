@@ -246,8 +246,9 @@ gdn_status gdn_short_conv_step(const void* x, const float* w, float* conv_state,
  *                 bytes, 256-byte aligned, owned by the caller; its contents
  *                 on entry do not matter and are garbage on return. It holds
  *                 the state at the start of every block of 32 tokens
- *                 (64 KB per block and value head) and, when H_v > H_qk,
- *                 the per-value-head parts of dq and dk.
+ *                 (64 KB per block and value head), the forward pass's error
+ *                 vector of every token (512 B per token and value head) and,
+ *                 when H_v > H_qk, the per-value-head parts of dq and dk.
  *
  * All arithmetic is fp32 (bf16 inputs are widened exactly). The kernel
  * replays the forward from the checkpoints, so o and the final state of the
@@ -272,8 +273,10 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v,
  * gdn_chunk_bwd_workspace_size -- bytes of workspace gdn_chunk_bwd needs for
  * these sizes (host only, launches nothing). It depends on N, T_total and
  * the head counts only, not on cu_seqlens: with blocks of 32 tokens,
- * H_v * (T_total / 32 + N + 1) states of d_k * d_v fp32, plus
- * 2 * T_total * H_v * d_k fp32 when H_v > H_qk. Returns 0 for invalid sizes.
+ * H_v * (T_total / 32 + N + 1) states of d_k * d_v fp32, T_total * H_v *
+ * (d_v + 1) fp32 for the per-token values the forward sweep hands to the
+ * reverse sweep, plus 2 * T_total * H_v * d_k fp32 when H_v > H_qk (each part
+ * rounded up to 256 bytes). Returns 0 for invalid sizes.
  */
 size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
                                     int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v);
@@ -293,7 +296,8 @@ size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
  *
  * Limit: the problem must satisfy gdn_chunk_bwd_workspace_size(...) <=
  * GDN_BWD_STATIC_SCRATCH_BYTES (for example one sequence of up to 4096
- * tokens with 4 value heads and no head sharing: 4 * 133 states of 64 KB);
+ * tokens with 4 value heads and no head sharing: 4 * 130 states of 64 KB
+ * plus 8.5 MB of per-token values, 40.6 MiB in all);
  * larger problems return GDN_ERR_UNSUPPORTED before touching the device.
  * The first call on each device looks up the array's device address (with
  * that device current) and caches it; make that first call before any

@@ -260,9 +260,12 @@ def test_chunk_bwd_host_validation(L, kw, status):
 def test_chunk_bwd_workspace_size(L):
     f = L.gdn_chunk_bwd_workspace_size
     st = 128 * 128 * 4
-    # checkpoints: H_v * (T/32 + N + 1) states; grouped heads add two [T, H_v, 128] fp32 parts
-    assert f(4, 16384, 16, 32, 128, 128) == 32 * (512 + 5) * st + 2 * 16384 * 32 * 128 * 4
-    assert f(1, 100, 4, 4, 128, 128) == 4 * (3 + 2) * st
+    up = lambda x: (x + 255) // 256 * 256
+    # checkpoints: H_v * (T/32 + N + 1) states; per token and value head the error
+    # vector and one scalar; grouped heads add two [T, H_v, 128] fp32 parts
+    assert f(4, 16384, 16, 32, 128, 128) == (32 * (512 + 5) * st + 2 * 16384 * 32 * 128 * 4
+                                             + 16384 * 32 * 128 * 4 + 16384 * 32 * 4)
+    assert f(1, 100, 4, 4, 128, 128) == 4 * (3 + 2) * st + 100 * 4 * 128 * 4 + up(100 * 4 * 4)
     assert f(0, 0, 1, 1, 128, 128) == 1 * st
     assert f(-1, 0, 1, 1, 128, 128) == 0 and f(1, 10, 3, 4, 128, 128) == 0
     assert gdn.chunk_bwd_workspace_size(4, 16384, 16, 32) == f(4, 16384, 16, 32, 128, 128)
