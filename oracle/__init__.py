@@ -16,6 +16,8 @@ numpy / torch CPU arrays into it and back.
                   depthwise conv, SiLU, per-head L2 norm), in ``prologue.py``
   recurrent_backward(...)  the gradient of the recurrence (reverse-order chain
                   rule, numpy fp64), in ``backward.py``
+  kda_recurrent(...)  the per-key-channel-decay variant (KDA), numpy fp64, in
+                  ``kda.py``
 
 Both return ``(o, S)``: with ``pairs=None`` o is [T_total, H_v, d_v] and S is
 [N, H_v, d_k, d_v] (float64 numpy); with ``pairs=[(n, h), ...]`` they are
@@ -36,6 +38,7 @@ import numpy as np
 
 from .backward import recurrent_backward  # noqa: F401
 from .epilogue import gated_rmsnorm, rms_normalize, sigmoid  # noqa: F401
+from .kda import kda_recurrent  # noqa: F401
 from .prologue import l2_normalize_groups, short_conv, short_conv_step, silu  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
