@@ -7,8 +7,9 @@ q/k/v, fp32 g/beta and state, chunk 64, zero initial state, bf16 output plus
 fp32 final states. value = tokens/s over all ranks. The same JSON line also
 carries the decode step (256 sequences x 32 heads x 128x128 fp32 states,
 1000 consecutive in-place steps, bf16 token inputs) in GB/s, the output
-epilogue and input prologue in GB/s, and the gradient of the prefill
-workload (gdn_chunk_bwd) in tokens/s against the fp32 CUDA-core peak.
+epilogue and input prologue in GB/s, the gradient of the prefill
+workload (gdn_chunk_bwd) in tokens/s against the fp32 CUDA-core peak, and the
+per-channel-decay variant (KDA) prefill and decode.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -316,6 +317,7 @@ def run_ours(args, world, rank, local):
     epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o)
     prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
     backward = None if args.skip_backward else run_backward(args, dev, peaks, world, w, dd)
+    kda = None if args.skip_kda else run_kda(args, dev, peaks, world, w, dd)
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
@@ -333,7 +335,7 @@ def run_ours(args, world, rank, local):
                    "l2": "inputs larger than L2 (126 MB) every step; no flush"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
         "clocks": clk.summary(), "decode": decode, "epilogue": epilogue, "prologue": prologue,
-        "backward": backward,
+        "backward": backward, "kda": kda,
     }
 
 
@@ -559,6 +561,79 @@ def run_backward(args, dev, peaks, world, w, dd):
                          "algorithmic_flops_per_launch": flops}}
 
 
+def run_kda(args, dev, peaks, world, w, dd):
+    """The per-channel-decay variant (KDA): the prefill workload with one
+    log-decay per key channel (g = -softplus(N(0,1) + 2) per channel), and
+    in-place decode steps on the decode workload's 256 x 32 states with
+    per-channel decays drawn per step."""
+    import gated_deltanet_recurrence_05_b300 as gdn
+    lengths = w["lengths"]
+    N, T = len(lengths), sum(lengths)
+    h_v, d_k, d_v = w["h_v"], w["d_k"], w["d_v"]
+    g = gdn_inputs.make_channel_decay((T, h_v, d_k), g_shift=2.0, seed=args.seed).to(dev)
+    o = torch.empty(T, h_v, d_v, dtype=torch.bfloat16, device=dev)
+    fs = torch.empty(N, h_v, d_k, d_v, dtype=torch.float32, device=dev)
+    cu = dd["cu_seqlens"]
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        gdn.kda_chunk_fwd(dd["q"], dd["k"], dd["v"], g, dd["beta"], dd["h0"], cu,
+                          num_seqs=None if cu is not None else N, out=o, final_state_out=fs, stream=stream)
+
+    def timed(fn, reps):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for i in range(reps):
+            fn(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if gdn.get_device_error() != 0:
+            raise RuntimeError("device error in KDA")
+        return max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+
+    for _ in range(3):
+        prefill()
+    reps = max(3, min(args.steps, 10))
+    us_pf = timed(lambda i: prefill(), reps)
+    flops = 6.0 * d_k * d_v * T * h_v   # S^T (a o k), S^T (a o q), the decayed rank-1 update
+    tfs = flops / (us_pf / 1e6) / 1e12
+
+    wl = gdn_inputs.WORKLOADS["decode"]
+    steps = 100
+    t = gdn_inputs.make_workload("decode", steps=steps, seed=args.seed)
+    tt = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in t.items()}
+    gd = gdn_inputs.make_channel_decay((steps, wl.num_seqs, wl.h_v, wl.d_k), seed=args.seed).to(dev)
+    state = tt["state"].clone()
+    od = torch.empty(wl.num_seqs, wl.h_v, wl.d_v, dtype=torch.bfloat16, device=dev)
+
+    def dstep(i):
+        gdn.kda_decode_step(tt["q"][i], tt["k"][i], tt["v"][i], gd[i], tt["beta"][i], state, out=od,
+                            stream=stream)
+
+    for i in range(3):
+        dstep(i)
+    state.copy_(tt["state"])
+    us_dec = timed(dstep, steps)
+    # the decode step's bytes with g per key channel instead of one per head
+    b = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v) + wl.num_seqs * wl.h_v * (wl.d_k - 1) * 4
+    gbs = b / (us_dec / 1e6) / 1e9
+    return {"prefill": {"workload": f"KDA prefill: the prefill workload (B={N}, T={T // N}) with per-channel "
+                                    f"fp32 log-decays [T, {h_v}, {d_k}], bf16 o, fp32 final states",
+                        "us_per_launch": us_pf, "tokens_per_s": T * world / (us_pf / 1e6), "gpu_launches": reps,
+                        "roofline": {"bound": "alu", "achieved": round(tfs, 2), "peak": round(SIMT_FP32_TFLOPS, 1),
+                                     "unit": "TFLOP/s", "frac": round(tfs / SIMT_FP32_TFLOPS, 4),
+                                     "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz",
+                                     "algorithmic_flops_per_launch": flops}},
+            "decode": {"workload": f"KDA decode: {wl.num_seqs} x {wl.h_v} states of 128x128 fp32, per-channel "
+                                   f"decays, {steps} in-place steps",
+                       "us_per_step": us_dec, "GB_per_s": gbs * world, "gpu_launches": steps,
+                       "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                                    "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                    "algorithmic_bytes_per_launch": int(b)}}}
+
+
 def run_reference(args, world, rank):
     """The oracle as it stands, timed on the host cores (bounded sample)."""
     if rank != 0:
@@ -600,6 +675,7 @@ def main(argv=None):
     ap.add_argument("--skip-epilogue", action="store_true", help="skip the epilogue and prologue lines")
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-backward", action="store_true", help="skip the gradient line")
+    ap.add_argument("--skip-kda", action="store_true", help="skip the per-channel-decay (KDA) lines")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)

@@ -72,6 +72,11 @@ def lib():
                                            I32, I32, I32, I32, I32, F, P]
         L.gdn_chunk_bwd_static.restype = ctypes.c_int
         L.gdn_chunk_bwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32]
+        L.gdn_kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32,
+                                        F, P]
+        L.gdn_kda_chunk_fwd.restype = ctypes.c_int
+        L.gdn_kda_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, F, P]
+        L.gdn_kda_decode_step.restype = ctypes.c_int
         L.gdn_chunk_bwd_workspace_size.restype = ctypes.c_size_t
         L.gdn_plan_seq_order.argtypes = [P, I32, P]
         L.gdn_plan_seq_order.restype = ctypes.c_int
@@ -221,6 +226,61 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
                              workspace.numel() * workspace.element_size(), _stream(stream))
     _check("gdn_chunk_bwd", st)
     return dq, dk, dv, dg, db, dh0
+
+
+def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                  initial_state: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None, *,
+                  num_seqs: Optional[int] = None, seq_order: Optional[torch.Tensor] = None,
+                  output_dtype: Optional[torch.dtype] = None, scale: float = 0.0, output_final_state: bool = True,
+                  out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None, stream=None):
+    """Prefill of the per-channel-decay rule (KDA; see include/gdn.h). As
+    ``chunk_fwd`` except g: [T, H_v, d_k] fp32 (one log-decay per key channel)."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        _dev(t, name)
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    if cu_seqlens is not None:
+        _dev(cu_seqlens, "cu_seqlens")
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = 1 if num_seqs is None else int(num_seqs)
+    for name, t in (("seq_order", seq_order), ("initial_state", initial_state)):
+        if t is not None:
+            _dev(t, name)
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("g and beta must be float32")
+    if tuple(g.shape) != (T, h_v, d_k):
+        raise ValueError("g must be [T, H_v, d_k]")
+    odt = output_dtype or v.dtype
+    o = out if out is not None else torch.empty((T, h_v, d_v), dtype=odt, device=v.device)
+    fs = None
+    if output_final_state:
+        fs = final_state_out if final_state_out is not None else torch.empty(
+            (N, h_v, d_k, d_v), dtype=torch.float32, device=v.device)
+    st = lib().gdn_kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                 _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(fs), N, T, h_qk, h_v, d_k,
+                                 d_v, _code(q), _code(o), float(scale), _stream(stream))
+    _check("gdn_kda_chunk_fwd", st)
+    return o, fs
+
+
+def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                    state: torch.Tensor, *, output_dtype: Optional[torch.dtype] = None, scale: float = 0.0,
+                    out: Optional[torch.Tensor] = None, stream=None):
+    """One token of KDA for N sequences, state updated in place. q, k
+    [N, H_qk, d_k]; v [N, H_v, d_v]; g [N, H_v, d_k] fp32; beta [N, H_v];
+    state [N, H_v, d_k, d_v] fp32. Returns o [N, H_v, d_v]."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
+        _dev(t, name)
+    N, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    o = out if out is not None else torch.empty((N, h_v, d_v), dtype=output_dtype or v.dtype, device=v.device)
+    st = lib().gdn_kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o), N,
+                                   h_qk, h_v, d_k, d_v, _code(q), _code(o), float(scale), _stream(stream))
+    _check("gdn_kda_decode_step", st)
+    return o
 
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,

@@ -17,6 +17,7 @@
 #include "gdn_chunk_simt.cuh"
 #include "gdn_chunk_tc.cuh"
 #include "gdn_backward.cuh"
+#include "gdn_kda.cuh"
 
 namespace {
 
@@ -230,6 +231,35 @@ gdn_status launch_bwd(gdn::bwd::Args a, float* dq, float* dk, char* ws, const Bw
 }  // namespace
 
 
+namespace {
+
+template <typename TIn, typename TOut>
+gdn_status launch_kda_prefill(const gdn::kda::Args& a, cudaStream_t s) {
+    const long long blocks = (long long)a.num_seqs * a.h_v;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    const DevInfo di = dev_info();
+    if (di.smem_optin < (int)gdn::kda::SMEM_BYTES) return di.smem_optin <= 0 ? GDN_ERR_CUDA : GDN_ERR_UNSUPPORTED;
+    auto kern = gdn::kda::kda_prefill_kernel<TIn, TOut>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gdn::kda::SMEM_BYTES) !=
+        cudaSuccess)
+        return GDN_ERR_CUDA;
+    kern<<<(unsigned)blocks, gdn::kda::NT, gdn::kda::SMEM_BYTES, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename TIn, typename TOut>
+gdn_status launch_kda_decode(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             float* state, void* o, int N, int h_qk, int h_v, float scale, cudaStream_t s) {
+    const long long blocks = (long long)N * h_v;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    gdn::kda::kda_decode_d128_kernel<TIn, TOut><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const TIn*>(q), static_cast<const TIn*>(k), static_cast<const TIn*>(v), g, beta, state,
+        static_cast<TOut*>(o), h_qk, h_v, h_v / h_qk, scale);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
 // Scratch of gdn_chunk_bwd_static: a fixed device array in this module, so
 // that callers without an allocator can still take the gradient. Host code
 // must not use the symbol's name as a pointer; the device address comes from
@@ -268,7 +298,7 @@ const char* gdn_status_string(gdn_status s) {
     return "GDN_ERR_UNKNOWN";
 }
 
-int32_t gdn_version(void) { return 102; }
+int32_t gdn_version(void) { return 103; }
 
 gdn_status gdn_plan_seq_order(const int32_t* cu, int32_t num_seqs, int32_t* order_out) {
     if (num_seqs < 0 || (num_seqs > 0 && (cu == nullptr || order_out == nullptr))) return GDN_ERR_INVALID_ARG;
@@ -511,6 +541,61 @@ gdn_status gdn_chunk_bwd_static(const void* q, const void* k, const void* v, con
     return gdn_chunk_bwd(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq, dk, dv, dg,
                          dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, d_k, d_v, dtype_qkv, dtype_do,
                          scale, scratch, GDN_BWD_STATIC_SCRATCH_BYTES, stream);
+}
+
+gdn_status gdn_kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             const float* initial_state, const int32_t* cu_seqlens, const int32_t* seq_order,
+                             void* o, float* final_state, int32_t num_seqs, int64_t total_tokens, int32_t h_qk,
+                             int32_t h_v, int32_t d_k, int32_t d_v, int32_t dtype_qkv, int32_t dtype_o,
+                             float scale, void* stream) {
+    if (num_seqs < 0 || total_tokens < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
+    if (d_k != gdn::kda::D || d_v != gdn::kda::D) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+    if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g) || !ok_ptr(beta, 4) ||
+                             !ok_ptr(o, esize(dtype_o))))
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_opt(initial_state) || !ok_opt(final_state) || !ok_opt(cu_seqlens, 4) || !ok_opt(seq_order, 4))
+        return GDN_ERR_INVALID_ARG;
+    if (total_tokens == 0 && final_state == nullptr) return GDN_OK;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
+    gdn::kda::Args a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = initial_state; a.cu = cu_seqlens;
+    a.order = seq_order; a.o = o; a.hT = final_state; a.total = total_tokens;
+    a.eq_len = cu_seqlens ? 0 : total_tokens / num_seqs; a.num_seqs = num_seqs; a.h_qk = h_qk; a.h_v = h_v;
+    a.grp = h_v / h_qk; a.scale = scale;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bi = dtype_qkv == GDN_BF16, bo = dtype_o == GDN_BF16;
+    if (bi && bo) return launch_kda_prefill<__nv_bfloat16, __nv_bfloat16>(a, s);
+    if (bi) return launch_kda_prefill<__nv_bfloat16, float>(a, s);
+    if (bo) return launch_kda_prefill<float, __nv_bfloat16>(a, s);
+    return launch_kda_prefill<float, float>(a, s);
+}
+
+gdn_status gdn_kda_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                               float* state, void* o, int32_t num_seqs, int32_t h_qk, int32_t h_v, int32_t d_k,
+                               int32_t d_v, int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream) {
+    if (num_seqs < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
+    if (d_k != gdn::kda::D || d_v != gdn::kda::D) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return GDN_OK;
+    const uintptr_t ei = esize(dtype_qkv), eo = esize(dtype_o);
+    // q and k are read 4 elements at a time
+    if (!ok_ptr(q, 4 * ei) || !ok_ptr(k, 4 * ei) || !ok_ptr(v, ei) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) ||
+        !ok_ptr(state, 16) || !ok_ptr(o, eo))
+        return GDN_ERR_INVALID_ARG;
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool bi = dtype_qkv == GDN_BF16, bo = dtype_o == GDN_BF16;
+    if (bi && bo)
+        return launch_kda_decode<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, scale, s);
+    if (bi) return launch_kda_decode<__nv_bfloat16, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, scale, s);
+    if (bo) return launch_kda_decode<float, __nv_bfloat16>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, scale, s);
+    return launch_kda_decode<float, float>(q, k, v, g, beta, state, o, num_seqs, h_qk, h_v, scale, s);
 }
 
 #ifdef GDN_TRACE

@@ -37,7 +37,8 @@ from typing import Optional
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_workload", "make_grads"]
+__all__ = ["Workload", "WORKLOADS", "make_prefill", "make_decode", "make_workload", "make_grads",
+           "make_channel_decay"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -182,3 +183,12 @@ def make_grads(problem: dict, *, dtype: str = "f32", dht_std: float = 0.0, seed:
     if dht_std > 0:
         dht = torch.randn(n, v.shape[1], problem["q"].shape[2], v.shape[2], generator=gen) * dht_std
     return dict(do=do.to(_DT[dtype]).contiguous(), dht=dht)
+
+
+def make_channel_decay(shape, *, g_shift: float = 0.0, seed: int = 0) -> torch.Tensor:
+    """Per-key-channel log-decays for the per-channel-decay variant (KDA):
+    g = -softplus(N(0, 1) + g_shift) of the given shape ([T, H_v, d_k] for a
+    prefill, [N, H_v, d_k] for a decode step), fp32, from its own generator
+    seeded with ``seed + 104729``."""
+    gen = _gen(seed + 104729)
+    return (-torch.nn.functional.softplus(torch.randn(tuple(shape), generator=gen) + g_shift)).contiguous()

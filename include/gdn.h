@@ -282,6 +282,41 @@ size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
                                     int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v);
 
 /*
+ * gdn_kda_chunk_fwd / gdn_kda_decode_step -- the per-channel-decay variant
+ * of the rule (KDA). The pages name KDA only as the alternative linear mixer
+ * ("Qwen3.8 attention gate" page, blueprint component "Gated DeltaNet /
+ * KDA") without a definition; implemented is the rule above with one decay
+ * per key channel instead of one per head:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     o_t = scale * S_t^T q_t,   alpha_t = exp(g_t) in R^{d_k}
+ *
+ * (the decay applies before the delta read, as in the scalar rule; equal
+ * channels give the gated delta rule). Arguments as for gdn_chunk_fwd and
+ * gdn_decode_step except g, which is per key channel:
+ *   prefill: g [T_total, H_v, d_k] fp32     decode: g [N, H_v, d_k] fp32
+ * Both need d_k = d_v = 128 (GDN_ERR_UNSUPPORTED otherwise) and 16-byte
+ * aligned g. The prefill runs token by token on the fp32 CUDA cores (one CTA
+ * per sequence and value head, state in registers); the decode step reads
+ * and writes each state once, like gdn_decode_step.
+ */
+gdn_status gdn_kda_chunk_fwd(const void* q, const void* k, const void* v,
+                             const float* g, const float* beta,
+                             const float* initial_state, const int32_t* cu_seqlens,
+                             const int32_t* seq_order,
+                             void* o, float* final_state,
+                             int32_t num_seqs, int64_t total_tokens,
+                             int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                             int32_t dtype_qkv, int32_t dtype_o, float scale, void* stream);
+gdn_status gdn_kda_decode_step(const void* q, const void* k, const void* v,
+                               const float* g, const float* beta,
+                               float* state, void* o,
+                               int32_t num_seqs, int32_t h_qk, int32_t h_v,
+                               int32_t d_k, int32_t d_v,
+                               int32_t dtype_qkv, int32_t dtype_o, float scale,
+                               void* stream);
+
+/*
  * gdn_chunk_bwd_static -- gdn_chunk_bwd for callers that cannot allocate
  * device memory. (The paper has no counterpart: this is a library
  * convenience.) Some callers have no way to obtain a device buffer for the

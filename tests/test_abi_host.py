@@ -36,6 +36,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
                  "gdn_short_conv", "gdn_short_conv_step", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size",
+                 "gdn_chunk_bwd_static", "gdn_kda_chunk_fwd", "gdn_kda_decode_step",
                  "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
         assert need in names
@@ -269,3 +270,41 @@ def test_chunk_bwd_workspace_size(L):
     assert f(0, 0, 1, 1, 128, 128) == 1 * st
     assert f(-1, 0, 1, 1, 128, 128) == 0 and f(1, 10, 3, 4, 128, 128) == 0
     assert gdn.chunk_bwd_workspace_size(4, 16384, 16, 32) == f(4, 16384, 16, 32, 128, 128)
+
+
+def _kda(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, order=None, o=FAKE, hT=FAKE, N=2,
+             T=64, h_qk=2, h_v=4, d_k=128, d_v=128, dq=1, do=1, scale=0.0)
+    a.update(kw)
+    return L.gdn_kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["h0"], a["cu"], a["order"], a["o"],
+                               a["hT"], a["N"], a["T"], a["h_qk"], a["h_v"], a["d_k"], a["d_v"], a["dq"], a["do"],
+                               a["scale"], None)
+
+
+# Every case below has at least one invalid argument, so nothing is launched.
+@pytest.mark.parametrize("kw,status", [
+    (dict(g=FAKE + 4), INVALID),                 # per-channel g is read 16 bytes at a time
+    (dict(q=None), INVALID),
+    (dict(hT=FAKE + 8), INVALID),
+    (dict(h_qk=3), INVALID),
+    (dict(dq=2), INVALID),
+    (dict(N=3, T=64), INVALID),
+    (dict(d_k=64, d_v=64), UNSUPPORTED),
+    (dict(N=0, T=0), OK),
+])
+def test_kda_chunk_fwd_host_validation(L, kw, status):
+    assert _kda(L, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(state=FAKE + 4), INVALID),
+    (dict(q=FAKE + 2), INVALID),                 # q, k are read 4 elements at a time
+    (dict(d_v=64), UNSUPPORTED),
+    (dict(N=0), OK),
+])
+def test_kda_decode_host_validation(L, kw, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, state=FAKE, o=FAKE, N=4, h_qk=2, h_v=4, d_k=128,
+             d_v=128, dq=1, do=1, scale=0.0)
+    a.update(kw)
+    assert L.gdn_kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state"], a["o"], a["N"], a["h_qk"],
+                                 a["h_v"], a["d_k"], a["d_v"], a["dq"], a["do"], a["scale"], None) == status
