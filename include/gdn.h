@@ -23,7 +23,9 @@
  *    v of gdn_chunk_fwd and every state pointer must be 16-byte aligned (TMA
  *    and 128-bit accesses); g, beta, cu_seqlens and seq_order need 4-byte
  *    alignment, o and the q/k/v of gdn_decode_step their element size.
- *    The caller owns every buffer; the library never allocates device memory.
+ *    The caller owns every buffer; no call allocates device memory (the one
+ *    fixed reservation is the scratch array of gdn_chunk_bwd_static, held by
+ *    every device that loads the library).
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
  *    the legacy default stream). Argument checks run on the host before any
  *    launch; on any error status nothing has been launched.
