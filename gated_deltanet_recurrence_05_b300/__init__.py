@@ -108,6 +108,30 @@ def _dev(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _shape(t: Optional[torch.Tensor], shape, name: str):
+    """Raise unless t (when given) has exactly this shape: the C ABI takes bare
+    pointers and sizes, so a tensor smaller than the sizes imply would be read
+    past its end."""
+    if t is not None and tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(int(x) for x in shape)}, got {tuple(t.shape)}")
+
+
+def _shapes_prefill(q, k, v, g, beta, N, h0=None, g_per_channel=False, h0_name="initial_state"):
+    """Shape checks shared by the prefill-style calls: q, k [T, H_qk, d_k];
+    v [T, H_v, d_v]; g [T, H_v] (or [T, H_v, d_k] per channel); beta [T, H_v];
+    h0 [N, H_v, d_k, d_v]. Returns (T, h_qk, h_v, d_k, d_v)."""
+    if q.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k must be [T, H_qk, d_k] and v [T, H_v, d_v]")
+    T, h_qk, d_k = q.shape
+    h_v, d_v = v.shape[1], v.shape[2]
+    _shape(k, q.shape, "k")
+    _shape(v, (T, h_v, d_v), "v")
+    _shape(g, (T, h_v, d_k) if g_per_channel else (T, h_v), "g")
+    _shape(beta, (T, h_v), "beta")
+    _shape(h0, (N, h_v, d_k, d_v), h0_name)
+    return T, h_qk, h_v, d_k, d_v
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -133,17 +157,17 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     [N+1] int32 CUDA tensor or None (then ``num_seqs`` equal-length sequences,
     default 1). Returns (o [T, H_v, d_v], final_state or None).
     """
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    T, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, N, initial_state)
+    _shape(seq_order, (N,), "seq_order")
+    _shape(out, (T, h_v, d_v), "out")
+    _shape(final_state_out, (N, h_v, d_k, d_v), "final_state_out")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         _dev(t, name)
-    T, h_qk, d_k = q.shape
-    h_v, d_v = v.shape[1], v.shape[2]
     if cu_seqlens is not None:
         _dev(cu_seqlens, "cu_seqlens")
         if cu_seqlens.dtype != torch.int32:
             raise TypeError("cu_seqlens must be int32")
-        N = cu_seqlens.numel() - 1
-    else:
-        N = 1 if num_seqs is None else int(num_seqs)
     if seq_order is not None:
         _dev(seq_order, "seq_order")
     if initial_state is not None:
@@ -185,17 +209,21 @@ def chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     here when None). ``out`` may give the six output tensors. Returns
     (dq, dk, dv, dg, dbeta, d_initial_state or None), all fp32.
     """
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    T, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, N, initial_state)
+    _shape(d_o, (T, h_v, d_v), "d_o")
+    _shape(d_final_state, (N, h_v, d_k, d_v), "d_final_state")
+    _shape(seq_order, (N,), "seq_order")
+    if out is not None:
+        for t, shp, name in zip(out, ((T, h_qk, d_k), (T, h_qk, d_k), (T, h_v, d_v), (T, h_v), (T, h_v),
+                                      (N, h_v, d_k, d_v)), ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")):
+            _shape(t, shp, f"out {name}")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("d_o", d_o)):
         _dev(t, name)
-    T, h_qk, d_k = q.shape
-    h_v, d_v = v.shape[1], v.shape[2]
     if cu_seqlens is not None:
         _dev(cu_seqlens, "cu_seqlens")
         if cu_seqlens.dtype != torch.int32:
             raise TypeError("cu_seqlens must be int32")
-        N = cu_seqlens.numel() - 1
-    else:
-        N = 1 if num_seqs is None else int(num_seqs)
     for name, t in (("seq_order", seq_order), ("initial_state", initial_state),
                     ("d_final_state", d_final_state)):
         if t is not None:
@@ -235,24 +263,22 @@ def kda_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None, stream=None):
     """Prefill of the per-channel-decay rule (KDA; see include/gdn.h). As
     ``chunk_fwd`` except g: [T, H_v, d_k] fp32 (one log-decay per key channel)."""
+    N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
+    T, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, N, initial_state, g_per_channel=True)
+    _shape(seq_order, (N,), "seq_order")
+    _shape(out, (T, h_v, d_v), "out")
+    _shape(final_state_out, (N, h_v, d_k, d_v), "final_state_out")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
         _dev(t, name)
-    T, h_qk, d_k = q.shape
-    h_v, d_v = v.shape[1], v.shape[2]
     if cu_seqlens is not None:
         _dev(cu_seqlens, "cu_seqlens")
         if cu_seqlens.dtype != torch.int32:
             raise TypeError("cu_seqlens must be int32")
-        N = cu_seqlens.numel() - 1
-    else:
-        N = 1 if num_seqs is None else int(num_seqs)
     for name, t in (("seq_order", seq_order), ("initial_state", initial_state)):
         if t is not None:
             _dev(t, name)
     if g.dtype != torch.float32 or beta.dtype != torch.float32:
         raise TypeError("g and beta must be float32")
-    if tuple(g.shape) != (T, h_v, d_k):
-        raise ValueError("g must be [T, H_v, d_k]")
     odt = output_dtype or v.dtype
     o = out if out is not None else torch.empty((T, h_v, d_v), dtype=odt, device=v.device)
     fs = None
@@ -272,10 +298,11 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     """One token of KDA for N sequences, state updated in place. q, k
     [N, H_qk, d_k]; v [N, H_v, d_v]; g [N, H_v, d_k] fp32; beta [N, H_v];
     state [N, H_v, d_k, d_v] fp32. Returns o [N, H_v, d_v]."""
+    N, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, q.shape[0], state, g_per_channel=True,
+                                             h0_name="state")
+    _shape(out, (N, h_v, d_v), "out")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
         _dev(t, name)
-    N, h_qk, d_k = q.shape
-    h_v, d_v = v.shape[1], v.shape[2]
     o = out if out is not None else torch.empty((N, h_v, d_v), dtype=output_dtype or v.dtype, device=v.device)
     st = lib().gdn_kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(o), N,
                                    h_qk, h_v, d_k, d_v, _code(q), _code(o), float(scale), _stream(stream))
@@ -294,10 +321,10 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tens
     RMSNorm epilogue (``gated_rmsnorm``), fused into the decode kernel for
     d_k = d_v = 128; ``norm_weight`` [d_v] fp32 is its zero-centred weight.
     """
+    N, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, q.shape[0], state, h0_name="state")
+    _shape(out, (N, h_v, d_v), "out")
     for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("state", state)):
         _dev(t, name)
-    N, h_qk, d_k = q.shape
-    h_v, d_v = v.shape[1], v.shape[2]
     odt = output_dtype or v.dtype
     o = out if out is not None else torch.empty((N, h_v, d_v), dtype=odt, device=v.device)
     if gate is None:

@@ -308,3 +308,28 @@ def test_kda_decode_host_validation(L, kw, status):
     a.update(kw)
     assert L.gdn_kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["state"], a["o"], a["N"], a["h_qk"],
                                  a["h_v"], a["d_k"], a["d_v"], a["dq"], a["do"], a["scale"], None) == status
+
+
+def test_binding_rejects_bad_shapes():
+    """Shapes are checked in the binding before anything reaches the C ABI
+    (which only sees pointers): a too-small tensor raises ValueError."""
+    T, hq, hv, d = 6, 1, 2, 8
+    q = torch.zeros(T, hq, d)
+    v = torch.zeros(T, hv, d)
+    g = torch.zeros(T, hv)
+    with pytest.raises(ValueError, match="g must"):
+        gdn.chunk_fwd(q, q, v, g[:, :1], g)
+    with pytest.raises(ValueError, match="initial_state"):
+        gdn.chunk_fwd(q, q, v, g, g, torch.zeros(1, hv, d, d - 1))
+    with pytest.raises(ValueError, match="d_o"):
+        gdn.chunk_bwd(q, q, v, g, g, v[:5])
+    with pytest.raises(ValueError, match="d_final_state"):
+        gdn.chunk_bwd(q, q, v, g, g, v, None, torch.zeros(2, hv, d, d))
+    with pytest.raises(ValueError, match="g must"):
+        gdn.kda_chunk_fwd(q, q, v, g, g)
+    with pytest.raises(ValueError, match="g must"):
+        gdn.kda_decode_step(q[:2], q[:2], v[:2], torch.zeros(2, hv, d - 1), g[:2], torch.zeros(2, hv, d, d))
+    with pytest.raises(ValueError, match="state must"):
+        gdn.decode_step(q[:2], q[:2], v[:2], g[:2], g[:2], torch.zeros(3, hv, d, d))
+    with pytest.raises(ValueError, match="k must"):
+        gdn.chunk_fwd(q, q[:, :, :4], v, g, g)
