@@ -1,7 +1,7 @@
 // Backward pass of the gated delta rule (the gradient needed to train the
 // token mixer: "On the Design of Qwen3.8-Next Architecture", arXiv abstract,
-// which weighs every change by its cost in training as well as in prefill and
-// decode). The forward rule is the one of "Qwen3.8-Next design: hybrid
+// which weighs every change by its training cost next to its prefill and
+// decode cost). The forward rule is the one of "Qwen3.8-Next design: hybrid
 // attention, residuals and n-gram embeddings" (podcast transcript, segment 14):
 //
 //   e_t = v_t - a_t S_{t-1}^T k_t,  S_t = a_t S_{t-1} + b_t k_t e_t^T,  o_t = scale S_t^T q_t

@@ -264,10 +264,14 @@ EDITS = {
 
 
 def _variant(old, new):
+    """The oracle's source with one edit in the recurrent form (the part of the
+    module before the chunked form), bound as a new module."""
     src = inspect.getsource(backward_module)
-    assert src.count(old) == 1, old
+    cut = src.index("def _pair_chunked_backward")
+    head, tail = src[:cut], src[cut:]
+    assert head.count(old) == 1, old
     ns = {"__name__": "backward_variant"}
-    exec(compile(src.replace(old, new), "backward_variant", "exec"), ns)
+    exec(compile(head.replace(old, new) + tail, "backward_variant", "exec"), ns)
     return ns["recurrent_backward"]
 
 
@@ -282,3 +286,50 @@ def test_planted_mistakes(edit):
             except (AssertionError, ValueError, FloatingPointError):
                 failed.append(pin.__name__)
     assert failed, f"no pin catches {edit}"
+
+
+# ----------------------------------------------------------------------------
+# the chunkwise form of the gradient: equal to the pinned recurrent form
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 16, 64, 200])
+def test_chunked_backward_equals_recurrent(chunk):
+    """The WY algebra differentiated chunk by chunk (oracle.chunked_backward)
+    equals the reverse-order chain rule on ragged varlen + GQA inputs with
+    S_0 and dS_T, for chunk sizes from 1 to longer than any sequence."""
+    P = _problem(7, lens=(5, 0, 37, 64, 70), h_qk=1, h_v=2, d_k=8, d_v=6)
+    ref = _call(oracle.recurrent_backward, P)
+    got = oracle.chunked_backward(P["q"], P["k"], P["v"], P["g"], P["beta"], P["do"], h0=P["h0"],
+                                  dht=P["dht"], cu_seqlens=P["cu"], chunk=chunk)
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        scale = np.abs(ref[name]).max()
+        np.testing.assert_allclose(got[name], ref[name], rtol=0, atol=1e-12 * scale, err_msg=name)
+
+
+CHUNK_EDITS = {
+    "no_transpose_in_dDelta": ("dDelta = scale * P.T @ dO + Kd @ D", "dDelta = scale * P @ dO + Kd @ D"),
+    "dA_sign": ("dA = np.tril(-T.T @ dT @ T.T, -1)", "dA = np.tril(T.T @ dT @ T.T, -1)"),
+    "dA_diagonal_kept": ("dA = np.tril(-T.T @ dT @ T.T, -1)", "dA = np.tril(-T.T @ dT @ T.T)"),
+    "dK_missing_transpose_term": ("dKc += E @ K + E.T @ K", "dKc += E @ K"),
+    "dS0_missing_state_term": ("dS0 = gam[-1] * D + scale", "dS0 = D + scale"),
+    "dbeta_missing_A_term": ("dbc += np.sum(dA * Gam * KK, axis=1)", "dbc += 0.0"),
+    "P_strict_lower": ("P = np.tril(Gam * (Q @ K.T))", "P = np.tril(Gam * (Q @ K.T), -1)"),
+}
+
+
+@pytest.mark.parametrize("edit", list(CHUNK_EDITS), ids=list(CHUNK_EDITS))
+def test_chunked_backward_planted_mistakes(edit):
+    old, new = CHUNK_EDITS[edit]
+    src = inspect.getsource(backward_module)
+    cut = src.index("def _pair_chunked_backward")
+    head, tail = src[:cut], src[cut:]
+    assert tail.count(old) == 1, old
+    ns = {"__name__": "backward_variant"}
+    exec(compile(head + tail.replace(old, new), "backward_variant", "exec"), ns)
+    P = _problem(8, lens=(9, 20), h_qk=1, h_v=2, d_k=5, d_v=4)
+    ref = _call(oracle.recurrent_backward, P)
+    got = ns["chunked_backward"](P["q"], P["k"], P["v"], P["g"], P["beta"], P["do"], h0=P["h0"], dht=P["dht"],
+                                 cu_seqlens=P["cu"], chunk=8)
+    worst = max(float(np.abs(got[n] - ref[n]).max() / np.abs(ref[n]).max())
+                for n in ("dq", "dk", "dv", "dg", "dbeta", "dh0"))
+    assert worst > 1e-6, f"{edit} not caught ({worst:.1e})"
