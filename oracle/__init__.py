@@ -38,7 +38,7 @@ import numpy as np
 
 from .backward import chunked_backward, recurrent_backward  # noqa: F401
 from .epilogue import gated_rmsnorm, rms_normalize, sigmoid  # noqa: F401
-from .kda import kda_recurrent  # noqa: F401
+from .kda import kda_chunked, kda_recurrent  # noqa: F401
 from .prologue import l2_normalize_groups, short_conv, short_conv_step, silu  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

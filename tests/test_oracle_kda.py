@@ -120,10 +120,14 @@ EDITS = {
 
 
 def _variant(old, new):
+    """The oracle's source with one edit in the recurrent form (the part of the
+    module before the chunked form), bound as a new module."""
     src = inspect.getsource(kda_module)
-    assert src.count(old) == 1, old
+    cut = src.index("def _pair_chunked")
+    head, tail = src[:cut], src[cut:]
+    assert head.count(old) == 1, old
     ns = {"__name__": "kda_variant"}
-    exec(compile(src.replace(old, new), "kda_variant", "exec"), ns)
+    exec(compile(head.replace(old, new) + tail, "kda_variant", "exec"), ns)
     return ns["kda_recurrent"]
 
 
@@ -138,3 +142,46 @@ def test_planted_mistakes(edit):
             except (AssertionError, ValueError, IndexError, FloatingPointError):
                 failed.append(pin.__name__)
     assert failed, f"no pin catches {edit}"
+
+
+# the chunkwise form (per-channel decay inside the inner products)
+
+def _chunk_problem(seed):
+    q, k, v, beta, h0, cu, rng = _rand(seed, (5, 0, 37, 64, 70), 1, 2, 8, 6)
+    g = -rng.uniform(0.0, 1.2, (len(q), 2, 8))
+    return q, k, v, g, beta, h0, cu
+
+
+@pytest.mark.parametrize("chunk", [1, 2, 3, 16, 64, 200])
+def test_kda_chunked_equals_recurrent(chunk):
+    q, k, v, g, beta, h0, cu = _chunk_problem(5)
+    o_ref, S_ref = oracle.kda_recurrent(q, k, v, g, beta, h0=h0, cu_seqlens=cu)
+    o, S = oracle.kda_chunked(q, k, v, g, beta, h0=h0, cu_seqlens=cu, chunk=chunk)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12 * np.abs(o_ref).max())
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-12 * np.abs(S_ref).max())
+
+
+CHUNK_EDITS = {
+    "scalar_decay_per_row": ('E = np.where(lower[:, :, None], np.exp(np.where(lower[:, :, None], diff, 0.0)), 0.0)',
+                             'E = np.where(lower[:, :, None], np.exp(np.where(lower[:, :, None], diff, 0.0)).mean(-1, keepdims=True), 0.0)'),
+    "P_strict_lower": ("np.tril(QK) @ U", "np.tril(QK, -1) @ U"),
+    "A_diagonal_kept": ("A = np.tril(bb[:, None] * KK, -1)", "A = np.tril(bb[:, None] * KK)"),
+    "state_decay_missing": ("S[...] = np.exp(G[-1])[:, None] * S +", "S[...] = S +"),
+    "query_decay_missing": ("o[c0:c1] = scale * ((Q * np.exp(G)) @ S", "o[c0:c1] = scale * (Q @ S"),
+}
+
+
+@pytest.mark.parametrize("edit", list(CHUNK_EDITS), ids=list(CHUNK_EDITS))
+def test_kda_chunked_planted_mistakes(edit):
+    old, new = CHUNK_EDITS[edit]
+    src = inspect.getsource(kda_module)
+    cut = src.index("def _pair_chunked")
+    head, tail = src[:cut], src[cut:]
+    assert tail.count(old) == 1, old
+    ns = {"__name__": "kda_variant"}
+    exec(compile(head + tail.replace(old, new), "kda_variant", "exec"), ns)
+    q, k, v, g, beta, h0, cu = _chunk_problem(6)
+    o_ref, S_ref = oracle.kda_recurrent(q, k, v, g, beta, h0=h0, cu_seqlens=cu)
+    o, S = ns["kda_chunked"](q, k, v, g, beta, h0=h0, cu_seqlens=cu, chunk=16)
+    worst = max(np.abs(o - o_ref).max() / np.abs(o_ref).max(), np.abs(S - S_ref).max() / np.abs(S_ref).max())
+    assert worst > 1e-6, f"{edit} not caught ({worst:.1e})"
