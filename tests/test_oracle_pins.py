@@ -245,10 +245,30 @@ def pin_default_scale(orc):
     np.testing.assert_allclose(S, S1, rtol=0, atol=0)
 
 
+def pin_value_columns_separate(orc):
+    """Column j of the state evolves on its own (u_j = beta (v_j - alpha
+    (S^T k)_j), S_:j <- alpha S_:j + k u_j): running the rule on a slice of
+    the value columns (v and S_0 restricted to it) gives that slice of the
+    outputs and final states, in both forms. This is what lets a kernel
+    split d_v across CTAs."""
+    lens = [9, 14]
+    P = _rand_problem(total=sum(lens), lengths=lens, d_v=7, seed=71)
+    o, S = orc.recurrent(**P)
+    oc, Sc = orc.chunked(**P, chunk=4)
+    for js in (slice(0, 3), slice(3, 7), slice(5, 6)):
+        Q = dict(P, v=np.ascontiguousarray(P["v"][..., js]), h0=np.ascontiguousarray(P["h0"][..., js]))
+        o1, S1 = orc.recurrent(**Q)
+        np.testing.assert_allclose(o1, o[..., js], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(S1, S[..., js], rtol=1e-13, atol=1e-14)
+        o2, S2 = orc.chunked(**Q, chunk=4)
+        np.testing.assert_allclose(o2, oc[..., js], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(S2, Sc[..., js], rtol=1e-11, atol=1e-13)
+
+
 PINS = [pin_hand_example, pin_literal_matrix_form, pin_beta_zero_closed_form,
         pin_orthonormal_retrieval, pin_same_key_twice, pin_linearity, pin_gqa_grouping,
         pin_packing_and_resume, pin_chunked_equals_recurrent, pin_fast_decay_chunks,
-        pin_default_scale]
+        pin_default_scale, pin_value_columns_separate]
 
 
 class _Module:
