@@ -333,3 +333,38 @@ def test_binding_rejects_bad_shapes():
         gdn.decode_step(q[:2], q[:2], v[:2], g[:2], g[:2], torch.zeros(3, hv, d, d))
     with pytest.raises(ValueError, match="k must"):
         gdn.chunk_fwd(q, q[:, :, :4], v, g, g)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "gdn.h"
+int main(void) {
+    int32_t order[3];
+    const int32_t cu[4] = {0, 5, 17, 20};
+    gdn_status st = gdn_plan_seq_order(cu, 3, order);
+    printf("%d %s %zu %d %d %d %d\n", (int)gdn_version(), gdn_status_string(GDN_ERR_UNSUPPORTED),
+           gdn_chunk_bwd_workspace_size(1, 100, 4, 4, 128, 128), (int)st, order[0], order[1], order[2]);
+    return st == GDN_OK ? 0 : 1;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """include/gdn.h compiles as strict C11 (no C++ or torch types in the
+    boundary) and a C program links libgdn.so and calls its host-only entry
+    points."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "t.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "t"
+    libdir = os.path.dirname(gbuild.LIB)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-o", str(exe), str(src), "-L", libdir, "-lgdn", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == L.gdn_version()
+    assert out[1] == "GDN_ERR_UNSUPPORTED"
+    assert int(out[2]) == L.gdn_chunk_bwd_workspace_size(1, 100, 4, 4, 128, 128)
+    assert out[3:] == ["0", "1", "0", "2"]   # lengths 5, 12, 3: longest first
