@@ -72,6 +72,8 @@ def lib():
                                            I32, I32, I32, I32, I32, F, P]
         L.gdn_chunk_bwd_static.restype = ctypes.c_int
         L.gdn_chunk_bwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32]
+        L.gdn_chunk_fwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, I32]
+        L.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
         L.gdn_kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, I32, I32,
                                         F, P]
         L.gdn_kda_chunk_fwd.restype = ctypes.c_int
@@ -186,6 +188,14 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
                              FLAG_FORCE_SIMT if force_simt else 0, _stream(stream))
     _check("gdn_chunk_fwd", st)
     return o, fs
+
+
+def chunk_fwd_workspace_size(num_seqs: int, total_tokens: int, h_qk: int, h_v: int, d_k: int = 128,
+                             d_v: int = 128, dtype: torch.dtype = torch.bfloat16) -> int:
+    """Bytes of device workspace ``chunk_fwd`` needs for these sizes (0: the
+    prefill keeps every intermediate on chip)."""
+    return int(lib().gdn_chunk_fwd_workspace_size(int(num_seqs), int(total_tokens), int(h_qk), int(h_v),
+                                                  int(d_k), int(d_v), BF16 if dtype == torch.bfloat16 else F32))
 
 
 def chunk_bwd_workspace_size(num_seqs: int, total_tokens: int, h_qk: int, h_v: int, d_k: int = 128,

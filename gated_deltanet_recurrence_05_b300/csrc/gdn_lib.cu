@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <mutex>
 #include <numeric>
+#include <utility>
 #include <vector>
 
 #include "../../include/gdn.h"
@@ -260,27 +261,109 @@ gdn_status launch_kda_decode(const void* q, const void* k, const void* v, const 
 
 }  // namespace
 
+namespace {
+
+// Host checks of gdn_chunk_bwd and gdn_chunk_bwd_static (everything except
+// the scratch memory), in the order the header documents. GDN_OK with
+// num_seqs == 0 means there is nothing to do.
+gdn_status bwd_check(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const float* initial_state, const int32_t* cu_seqlens, const int32_t* seq_order,
+                     const void* d_o, const float* d_final_state, const float* dq, const float* dk,
+                     const float* dv, const float* dg, const float* dbeta, const float* d_initial_state,
+                     int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                     int32_t dtype_qkv, int32_t dtype_do) {
+    if (!bwd_sizes_ok(num_seqs, total_tokens, h_qk, h_v, d_k, d_v)) return GDN_ERR_INVALID_ARG;
+    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_do)) return GDN_ERR_INVALID_ARG;
+    if (d_k != gdn::bwd::D || d_v != gdn::bwd::D) return GDN_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
+    if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
+    if (total_tokens > 0 &&
+        (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) || !ok_ptr(d_o) ||
+         !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv) || !ok_ptr(dg, 4) || !ok_ptr(dbeta, 4)))
+        return GDN_ERR_INVALID_ARG;
+    if (!ok_opt(initial_state) || !ok_opt(d_final_state) || !ok_opt(d_initial_state) || !ok_opt(cu_seqlens, 4) ||
+        !ok_opt(seq_order, 4))
+        return GDN_ERR_INVALID_ARG;
+    return GDN_OK;
+}
+
+// Launch of the backward kernels on a checked problem and a scratch region of
+// at least L.total bytes (256-byte aligned).
+gdn_status bwd_launch(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                      const float* initial_state, const int32_t* cu_seqlens, const int32_t* seq_order,
+                      const void* d_o, const float* d_final_state, float* dq, float* dk, float* dv, float* dg,
+                      float* dbeta, float* d_initial_state, int32_t num_seqs, int64_t total_tokens, int32_t h_qk,
+                      int32_t h_v, int32_t dtype_qkv, int32_t dtype_do, float scale, char* ws, const BwdLayout& L,
+                      cudaStream_t s) {
+    if (scale == 0.f) scale = 1.0f / sqrtf((float)gdn::bwd::D);
+    gdn::bwd::Args a{};
+    a.q = q; a.k = k; a.v = v; a.dout = d_o; a.g = g; a.beta = beta;
+    a.h0 = initial_state; a.dht = d_final_state; a.cu = cu_seqlens; a.order = seq_order;
+    a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = d_initial_state;
+    a.total = total_tokens; a.eq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
+    a.num_seqs = num_seqs; a.h_qk = h_qk; a.h_v = h_v; a.grp = h_v / h_qk; a.scale = scale;
+    const bool bq = dtype_qkv == GDN_BF16, bd = dtype_do == GDN_BF16;
+    if (bq && bd) return launch_bwd<__nv_bfloat16, __nv_bfloat16>(a, dq, dk, ws, L, s);
+    if (bq) return launch_bwd<__nv_bfloat16, float>(a, dq, dk, ws, L, s);
+    if (bd) return launch_bwd<float, __nv_bfloat16>(a, dq, dk, ws, L, s);
+    return launch_bwd<float, float>(a, dq, dk, ws, L, s);
+}
+
+}  // namespace
+
 // Scratch of gdn_chunk_bwd_static: a fixed device array in this module, so
 // that callers without an allocator can still take the gradient. Host code
 // must not use the symbol's name as a pointer; the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up with the device current.
 static __device__ __align__(256) unsigned char g_bwd_static_scratch[GDN_BWD_STATIC_SCRATCH_BYTES];
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_static_scratch_mu;
-void* g_static_scratch_ptr[kMaxDevices] = {};
+struct ScratchSlot { unsigned long long ctx_id = 0; void* ptr = nullptr; };
+ScratchSlot g_static_scratch[kMaxDevices];
 
+// Unique id of the current CUDA context (0 if it cannot be read). A device
+// reset destroys the primary context and a later call creates a new one with
+// a new id, into which the module (and with it the array) may load at
+// another address.
+unsigned long long current_context_id() {
+    static const auto fns = [] {
+        std::pair<PFN_cuCtxGetCurrent_v4000, PFN_cuCtxGetId_v12000> f{nullptr, nullptr};
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.first = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.second = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+        return f;
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (fns.first && fns.second && fns.first(&ctx) == CUDA_SUCCESS && ctx && fns.second(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of the array on the current device: looked up once per
+// device and context (the first call in a context does the lookup, with the
+// device current; a reset device gets a fresh lookup).
 gdn_status static_scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
+    const unsigned long long id = current_context_id();  // 0 before the context exists
     std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-    if (g_static_scratch_ptr[dev] == nullptr) {
+    ScratchSlot& slot = g_static_scratch[dev];
+    if (slot.ptr == nullptr || id == 0 || slot.ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_bwd_static_scratch) != cudaSuccess || p == nullptr) return GDN_ERR_CUDA;
-        g_static_scratch_ptr[dev] = p;
+        slot.ptr = p;
+        slot.ctx_id = current_context_id();  // the lookup has made the context current
     }
-    *out = g_static_scratch_ptr[dev];
+    *out = slot.ptr;
     return GDN_OK;
 }
 }  // namespace
@@ -480,6 +563,12 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     return launch_simt<float, float>(a, smem, s);
 }
 
+size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v,
+                                    int32_t d_k, int32_t d_v, int32_t dtype_qkv) {
+    (void)num_seqs; (void)total_tokens; (void)h_qk; (void)h_v; (void)d_k; (void)d_v; (void)dtype_qkv;
+    return 0;  // both forward kernels keep every intermediate on chip
+}
+
 size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v,
                                     int32_t d_k, int32_t d_v) {
     if (!bwd_sizes_ok(num_seqs, total_tokens, h_qk, h_v, d_k, d_v) || total_tokens > 0x7fffffffLL) return 0;
@@ -493,35 +582,15 @@ gdn_status gdn_chunk_bwd(const void* q, const void* k, const void* v, const floa
                          int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
                          int32_t dtype_qkv, int32_t dtype_do, float scale, void* workspace,
                          size_t workspace_bytes, void* stream) {
-    if (!bwd_sizes_ok(num_seqs, total_tokens, h_qk, h_v, d_k, d_v)) return GDN_ERR_INVALID_ARG;
-    if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_do)) return GDN_ERR_INVALID_ARG;
-    if (d_k != gdn::bwd::D || d_v != gdn::bwd::D) return GDN_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
-    if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
-    if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
-    if (total_tokens > 0 &&
-        (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g, 4) || !ok_ptr(beta, 4) || !ok_ptr(d_o) ||
-         !ok_ptr(dq) || !ok_ptr(dk) || !ok_ptr(dv) || !ok_ptr(dg, 4) || !ok_ptr(dbeta, 4)))
-        return GDN_ERR_INVALID_ARG;
-    if (!ok_opt(initial_state) || !ok_opt(d_final_state) || !ok_opt(d_initial_state) || !ok_opt(cu_seqlens, 4) ||
-        !ok_opt(seq_order, 4))
-        return GDN_ERR_INVALID_ARG;
+    const gdn_status st = bwd_check(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq,
+                                    dk, dv, dg, dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, d_k, d_v,
+                                    dtype_qkv, dtype_do);
+    if (st != GDN_OK || num_seqs == 0) return st;
     const BwdLayout L = bwd_layout(num_seqs, total_tokens, h_qk, h_v);
     if (!ok_ptr(workspace, 256) || workspace_bytes < L.total) return GDN_ERR_INVALID_ARG;
-    if (scale == 0.f) scale = 1.0f / sqrtf((float)d_k);
-    gdn::bwd::Args a{};
-    a.q = q; a.k = k; a.v = v; a.dout = d_o; a.g = g; a.beta = beta;
-    a.h0 = initial_state; a.dht = d_final_state; a.cu = cu_seqlens; a.order = seq_order;
-    a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = d_initial_state;
-    a.total = total_tokens; a.eq_len = cu_seqlens ? 0 : total_tokens / num_seqs;
-    a.num_seqs = num_seqs; a.h_qk = h_qk; a.h_v = h_v; a.grp = h_v / h_qk; a.scale = scale;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* ws = static_cast<char*>(workspace);
-    const bool bq = dtype_qkv == GDN_BF16, bd = dtype_do == GDN_BF16;
-    if (bq && bd) return launch_bwd<__nv_bfloat16, __nv_bfloat16>(a, dq, dk, ws, L, s);
-    if (bq) return launch_bwd<__nv_bfloat16, float>(a, dq, dk, ws, L, s);
-    if (bd) return launch_bwd<float, __nv_bfloat16>(a, dq, dk, ws, L, s);
-    return launch_bwd<float, float>(a, dq, dk, ws, L, s);
+    return bwd_launch(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq, dk, dv, dg,
+                      dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, dtype_qkv, dtype_do, scale,
+                      static_cast<char*>(workspace), L, static_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_chunk_bwd_static(const void* q, const void* k, const void* v, const float* g,
@@ -530,17 +599,20 @@ gdn_status gdn_chunk_bwd_static(const void* q, const void* k, const void* v, con
                                 float* dk, float* dv, float* dg, float* dbeta, float* d_initial_state,
                                 int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k,
                                 int32_t d_v, int32_t dtype_qkv, int32_t dtype_do, float scale, void* stream) {
-    // size checks on the host first: nothing touches the device for a rejected call
-    const size_t need = gdn_chunk_bwd_workspace_size(num_seqs, total_tokens, h_qk, h_v, d_k, d_v);
-    if (need == 0) return GDN_ERR_INVALID_ARG;
-    if (d_k != gdn::bwd::D || d_v != gdn::bwd::D) return GDN_ERR_UNSUPPORTED;
-    if (need > GDN_BWD_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED;
+    // the same host checks as gdn_chunk_bwd, in the same order, then the size
+    // limit of the array: nothing touches the device for a rejected call
+    const gdn_status st = bwd_check(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq,
+                                    dk, dv, dg, dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, d_k, d_v,
+                                    dtype_qkv, dtype_do);
+    if (st != GDN_OK || num_seqs == 0) return st;
+    const BwdLayout L = bwd_layout(num_seqs, total_tokens, h_qk, h_v);
+    if (L.total > GDN_BWD_STATIC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED;
     void* scratch = nullptr;
-    const gdn_status st = static_scratch_address(&scratch);
-    if (st != GDN_OK) return st;
-    return gdn_chunk_bwd(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq, dk, dv, dg,
-                         dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, d_k, d_v, dtype_qkv, dtype_do,
-                         scale, scratch, GDN_BWD_STATIC_SCRATCH_BYTES, stream);
+    const gdn_status sa = static_scratch_address(&scratch);
+    if (sa != GDN_OK) return sa;
+    return bwd_launch(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, d_o, d_final_state, dq, dk, dv, dg,
+                      dbeta, d_initial_state, num_seqs, total_tokens, h_qk, h_v, dtype_qkv, dtype_do, scale,
+                      static_cast<char*>(scratch), L, static_cast<cudaStream_t>(stream));
 }
 
 gdn_status gdn_kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,

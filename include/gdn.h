@@ -111,6 +111,24 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v,
                          void* stream);
 
 /*
+ * gdn_chunk_fwd_workspace_size -- bytes of device scratch that gdn_chunk_fwd
+ * needs for these sizes (host only, launches nothing). It is 0 for every
+ * problem: both prefill kernels keep all per-chunk intermediates (the
+ * triangular system of each chunk, its errors and the fp32 state) in
+ * registers, shared memory and tensor memory, so gdn_chunk_fwd takes no
+ * workspace argument. The query exists so that a caller which sizes the
+ * scratch of every call of a layer before running it can treat the prefill
+ * like the gradient (gdn_chunk_bwd_workspace_size). The arguments are those of
+ * gdn_chunk_fwd; sizes that gdn_chunk_fwd would reject also give 0.
+ * (The operation is the prefill of the gated delta rule described in the
+ * podcast episode "Qwen3.8-Next design: hybrid attention, residuals and
+ * n-gram embeddings", transcript segment 14.)
+ */
+size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
+                                    int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                                    int32_t dtype_qkv);
+
+/*
  * gdn_decode_step -- one token of the recurrence for N independent sequences,
  * updating the states in place (one read and one write of each state).
  *
@@ -337,8 +355,10 @@ gdn_status gdn_kda_decode_step(const void* q, const void* k, const void* v,
  * plus 8.5 MB of per-token values, 40.6 MiB in all);
  * larger problems return GDN_ERR_UNSUPPORTED before touching the device.
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any
- * stream capture. All calls on a device share the one array and it keeps
+ * that device current) and caches it for that device's context; make that
+ * first call before any stream capture. A device reset (cudaDeviceReset)
+ * ends the context, and the first call in the new context looks the address
+ * up again. All calls on a device share the one array and it keeps
  * whatever the last call left there (nothing in it needs to start at zero):
  * calls whose executions overlap on the GPU (other streams, other threads)
  * race on it and give wrong results, so serialise them.

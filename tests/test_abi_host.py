@@ -36,6 +36,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
                  "gdn_short_conv", "gdn_short_conv_step", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size",
+                 "gdn_chunk_fwd_workspace_size",
                  "gdn_chunk_bwd_static", "gdn_kda_chunk_fwd", "gdn_kda_decode_step",
                  "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
@@ -272,6 +273,43 @@ def test_chunk_bwd_workspace_size(L):
     assert gdn.chunk_bwd_workspace_size(4, 16384, 16, 32) == f(4, 16384, 16, 32, 128, 128)
 
 
+def test_chunk_fwd_workspace_size_is_zero(L):
+    """The prefill keeps every intermediate on chip: no workspace for any size
+    (the prefill, long and varlen workloads, a tiny fp32 case, invalid sizes)."""
+    f = L.gdn_chunk_fwd_workspace_size
+    assert f(4, 16384, 16, 32, 128, 128, 1) == 0
+    assert f(1, 65536, 16, 32, 128, 128, 1) == 0
+    assert f(64, 243613, 16, 32, 128, 128, 1) == 0
+    assert f(1, 64, 2, 2, 16, 16, 0) == 0
+    assert f(-1, 0, 1, 1, 128, 128, 1) == 0
+    assert gdn.chunk_fwd_workspace_size(4, 16384, 16, 32) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=1 << 31, N=1), UNSUPPORTED),         # more tokens than int32 cu_seqlens can index
+    (dict(h_qk=3), INVALID),
+    (dict(N=-1), INVALID),
+    (dict(dq=5), INVALID),
+    (dict(d_k=64), UNSUPPORTED),
+    (dict(N=3, T=100), INVALID),                 # equal lengths need T % N == 0
+    (dict(g=FAKE + 2), INVALID),
+    (dict(N=0, T=0), OK),
+    (dict(N=0, T=4), INVALID),
+])
+def test_chunk_bwd_static_refuses_like_chunk_bwd(L, kw, status):
+    """The allocation-free gradient entry point runs the same host checks as
+    gdn_chunk_bwd, in the same order, so both give one status for one bad
+    argument (nothing reaches the device in any case below)."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, order=None, do=FAKE, dht=None,
+             dq_=FAKE, dk_=FAKE, dv_=FAKE, dg_=FAKE, db_=FAKE, dh0=None, N=1, T=100, h_qk=4, h_v=4, d_k=128,
+             d_v=128, dq=1, ddo=1, scale=0.0)
+    a.update(kw)
+    args = [a[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu", "order", "do", "dht", "dq_", "dk_", "dv_",
+                           "dg_", "db_", "dh0", "N", "T", "h_qk", "h_v", "d_k", "d_v", "dq", "ddo", "scale")]
+    assert L.gdn_chunk_bwd_static(*args, None) == status
+    assert L.gdn_chunk_bwd(*args, None, 0, None) == status
+
+
 def _kda(L, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, h0=None, cu=None, order=None, o=FAKE, hT=FAKE, N=2,
              T=64, h_qk=2, h_v=4, d_k=128, d_v=128, dq=1, do=1, scale=0.0)
@@ -342,8 +380,9 @@ int main(void) {
     int32_t order[3];
     const int32_t cu[4] = {0, 5, 17, 20};
     gdn_status st = gdn_plan_seq_order(cu, 3, order);
-    printf("%d %s %zu %d %d %d %d\n", (int)gdn_version(), gdn_status_string(GDN_ERR_UNSUPPORTED),
-           gdn_chunk_bwd_workspace_size(1, 100, 4, 4, 128, 128), (int)st, order[0], order[1], order[2]);
+    printf("%d %s %zu %d %d %d %d %zu\n", (int)gdn_version(), gdn_status_string(GDN_ERR_UNSUPPORTED),
+           gdn_chunk_bwd_workspace_size(1, 100, 4, 4, 128, 128), (int)st, order[0], order[1], order[2],
+           gdn_chunk_fwd_workspace_size(4, 16384, 16, 32, 128, 128, GDN_BF16));
     return st == GDN_OK ? 0 : 1;
 }
 """
@@ -367,4 +406,5 @@ def test_header_is_plain_c_and_links(L, tmp_path):
     assert int(out[0]) == L.gdn_version()
     assert out[1] == "GDN_ERR_UNSUPPORTED"
     assert int(out[2]) == L.gdn_chunk_bwd_workspace_size(1, 100, 4, 4, 128, 128)
-    assert out[3:] == ["0", "1", "0", "2"]   # lengths 5, 12, 3: longest first
+    assert out[3:7] == ["0", "1", "0", "2"]   # lengths 5, 12, 3: longest first
+    assert out[7] == "0"                       # the prefill needs no workspace
