@@ -5,7 +5,9 @@ One step = one chunked prefill forward (gdn_chunk_fwd) over the prefill
 workload: B=4 sequences x T=4096 tokens, H_qk=16, H_v=32, d_k=d_v=128, bf16
 q/k/v, fp32 g/beta and state, chunk 64, zero initial state, bf16 output plus
 fp32 final states. value = tokens/s over all ranks. The same JSON line also
-carries the decode step (256 sequences x 32 heads x 128x128 fp32 states,
+carries the two other prefill workloads, each measured the same way: `long`
+(B=1, T=65536, h0 ~ N(0, 0.02)) and `varlen` (64 packed sequences, lengths
+U{128..8192}, per-sequence initial states); the decode step (256 sequences x 32 heads x 128x128 fp32 states,
 1000 consecutive in-place steps, bf16 token inputs) in GB/s, the output
 epilogue and input prologue in GB/s, the gradient of the prefill
 workload (gdn_chunk_bwd) in tokens/s against the fp32 CUDA-core peak, and the
@@ -16,6 +18,12 @@ per-channel-decay variant (KDA) prefill and decode.
 Under torchrun (N > 1) every rank runs its own independent copy of the
 workload (the work shards by sequence with no exchange: weak scaling); the
 timed region is bracketed by barriers and the max over ranks is reported.
+Every timed leg records one CUDA event per launch on the launching stream and
+reports the mean over the bracketed region (the value), the median with a 95%
+confidence interval, and its first call in the process separately (cold).
+`e2e` runs the same call on host buffers: each step copies its inputs from
+pinned host memory and its outputs back, with the copies of one step
+overlapping the previous step's call.
 --impl reference times the fp64 CPU oracle (test infrastructure) on a bounded
 sample of the same workload on the host cores.
 """
@@ -24,6 +32,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -49,12 +58,21 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "chunk_tc_prefill_ncu.txt")
 
 
 # --------------------------------------------------------------------------- helpers
+PEAK_SOURCE = "fallback"
+WL = gdn_inputs.WORKLOADS
+
+
 def load_peaks():
+    """The machine's measured peaks (copy bandwidth, bf16 dense) or the fallback."""
+    global PEAK_SOURCE
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return json.load(f), "measured"
+            peaks = json.load(f)
+        PEAK_SOURCE = "measured"
+        return peaks
     except (OSError, ValueError):
-        return dict(PEAKS_FALLBACK), "fallback"
+        PEAK_SOURCE = "fallback"
+        return dict(PEAKS_FALLBACK)
 
 
 def kernel_sha():
@@ -205,6 +223,58 @@ def cu_of(w):
     return torch.tensor([0] + torch.cumsum(torch.tensor(w["lengths"]), 0).tolist(), dtype=torch.int32)
 
 
+# --------------------------------------------------------------------------- timing helpers
+def median_ci95(xs):
+    """Median of the samples and a distribution-free 95% confidence interval
+    for it: the order statistics (j, k) with P(j <= Binom(n, 1/2) < k) >= 0.95,
+    as narrow as possible and symmetric (for n < 6 no pair reaches 0.95 and
+    the interval is the whole range)."""
+    xs = sorted(float(x) for x in xs)
+    n = len(xs)
+    if n == 0:
+        return None
+    med = statistics.median(xs)
+    lo, hi = 0, n - 1
+    for j in range(n // 2, -1, -1):
+        k = n - 1 - j
+        cover = sum(math.comb(n, i) for i in range(j + 1, k + 1)) / 2.0 ** n
+        if cover >= 0.95:
+            lo, hi = j, k
+            break
+    return {"median": med, "ci95": [xs[lo], xs[hi]], "n": n, "ci_method": "order statistics (binomial)"}
+
+
+def timed_launches(fn, reps, stream, dev, world):
+    """Run fn(i) for i < reps on `stream` with one CUDA event before each call
+    and one after the last (all on the launching stream), bracketed by a
+    barrier and device synchronisations. Returns (mean ms per call over the
+    whole bracketed region, list of per-call ms)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(reps):
+        evs[i].record(stream)
+        fn(i)
+    evs[reps].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(reps)]
+    return evs[0].elapsed_time(evs[reps]) / reps, per
+
+
+def cold_call(fn, stream, dev):
+    """Time one call that nothing has warmed (first call of this workload in
+    the process): device time between events and host wall time to its end."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t = time.perf_counter()
+    e0.record(stream)
+    fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return {"device_ms": e0.elapsed_time(e1), "host_wall_ms": (time.perf_counter() - t) * 1e3}
+
+
 # --------------------------------------------------------------------------- oracle (CPU) leg
 def oracle_sample(w, target_s=12.0, threads=0):
     """Time the fp64 oracle on a bounded sample of the workload: whole sequences
@@ -215,11 +285,14 @@ def oracle_sample(w, target_s=12.0, threads=0):
     cores = len(os.sched_getaffinity(0)) if threads <= 0 else threads
     N, hv = len(w["lengths"]), w["h_v"]
     cu = cu_of(w)
+    # the longest sequence first, so that the probe sees a representative pair
+    n0 = max(range(N), key=lambda n: w["lengths"][n])
     t = time.perf_counter()
     oracle.recurrent(w["q"], w["k"], w["v"], w["g"], w["beta"], h0=w["h0"], cu_seqlens=cu,
-                     pairs=[(0, 0)], threads=1)
-    one = time.perf_counter() - t
-    n_pairs = max(cores, int(target_s * cores / max(one, 1e-3)))
+                     pairs=[(n0, 0)], threads=1)
+    one = (time.perf_counter() - t) / max(w["lengths"][n0], 1)   # s per pair-token, one thread
+    mean_len = max(1.0, sum(w["lengths"]) / N)
+    n_pairs = max(cores, int(target_s * cores / max(one * mean_len, 1e-6)))
     n_pairs = max(1, min(n_pairs, N * hv))
     pairs = [(i // hv % N, i % hv) for i in range(n_pairs)]
     t = time.perf_counter()
@@ -232,12 +305,85 @@ def oracle_sample(w, target_s=12.0, threads=0):
         f"({pair_tokens} pair-tokens), fp64 recurrence, {dt:.1f} s")
 
 
+def oracle_baseline(w, target_s):
+    """The oracle on all host cores (bounded sample) and on one core (one
+    whole pair), both in tokens/s of the workload (pair-tokens / H_v)."""
+    import oracle
+    tok_s, cores, sample = oracle_sample(w, target_s=target_s)
+    N, hv = len(w["lengths"]), w["h_v"]
+    n0 = max(range(N), key=lambda n: w["lengths"][n])
+    t = time.perf_counter()
+    oracle.recurrent(w["q"], w["k"], w["v"], w["g"], w["beta"], h0=w["h0"], cu_seqlens=cu_of(w),
+                     pairs=[(n0, 0)], threads=1)
+    dt1 = time.perf_counter() - t
+    return {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "value_1thread": w["lengths"][n0] / hv / dt1,
+            "sample_1thread": f"one whole pair ({w['lengths'][n0]} tokens) on 1 thread, {dt1:.2f} s"}
+
+
 # --------------------------------------------------------------------------- GPU legs
-def run_ours(args, world, rank, local):
+def e2e_pipelined(host_in, dev_in, run, dev_out, host_out, steps, dev, world):
+    """End to end through the C ABI with HOST buffers: every step copies its
+    inputs from pinned host memory to the device, runs the call and copies its
+    outputs back to pinned host memory. Copies and calls go on three streams
+    with double-buffered device inputs and outputs, so that the copies of one
+    step overlap the call of the previous one (as a caller streaming batches
+    would run it). Returns seconds per step (max over ranks)."""
+    s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_run = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def go(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_run[b])       # the call of step i - 2 has read buffer b
+                for key, t in host_in.items():
+                    dev_in[b][key].copy_(t, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_run.wait_event(ev_in[b])
+            if i >= 2:
+                s_run.wait_event(ev_out[b])          # outputs b of step i - 2 are back on the host
+            run(dev_in[b], dev_out[b], s_run)
+            ev_run[b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_run[b])
+                for key, t in host_out.items():
+                    t.copy_(dev_out[b][key], non_blocking=True)
+                ev_out[b].record(s_out)
+        torch.cuda.synchronize(dev)
+
+    go(2)  # warm the streams and buffers
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    go(steps)
+    sec = (time.perf_counter() - t0) / steps
+    return max_over_ranks(sec, world, dev)
+
+
+def workload_config(name, w, world):
+    """The `config` object of a prefill line (the same for both arms)."""
+    lengths = w["lengths"]
+    N, T = len(lengths), sum(lengths)
+    seq = f"T={T // N}" if w["cu_seqlens"] is None else \
+        f"{N} packed sequences, lengths U{{{WL[name].len_lo}..{WL[name].len_hi}}} (seed 0: {T} tokens)"
+    h0 = "h0 ~ N(0, 0.02)" if w["h0"] is not None else "zero h0"
+    return {"workload": f"{name}: B={N}, {seq}, H_qk={w['h_qk']}, H_v={w['h_v']}, d_k=d_v={w['d_k']}, chunk 64, "
+                        f"bf16 q/k/v/o, fp32 g/beta/state, {h0}",
+            "global_batch": N * world, "seq_len": T // N, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (126 MB) every step; no flush"}
+
+
+def run_prefill_leg(args, name, dev, peaks, world, rank, steps, cpu_seconds, main=False):
+    """One prefill workload (gdn_chunk_fwd, bf16 o, fp32 final states) timed
+    over `steps` launches with inputs resident in HBM; plus its cold first call,
+    the median and 95% CI of the per-launch times, the roofline, the oracle on
+    the host cores and the pipelined end-to-end throughput through the C ABI."""
     import gated_deltanet_recurrence_05_b300 as gdn
-    dev = torch.device("cuda", local)
-    peaks, peak_kind = load_peaks()
-    w = gdn_inputs.make_workload(args.workload, seed=args.seed + rank)
+    w = gdn_inputs.make_workload(name, seed=args.seed + rank)
     lengths = w["lengths"]
     N, T = len(lengths), sum(lengths)
     dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
@@ -246,97 +392,114 @@ def run_ours(args, world, rank, local):
     fs = torch.empty(N, w["h_v"], w["d_k"], w["d_v"], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], dd["cu_seqlens"],
+    def call(inp, o_, fs_, s_):
+        gdn.chunk_fwd(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp.get("h0"), dd["cu_seqlens"],
                       num_seqs=None if w["cu_seqlens"] is not None else N, seq_order=order,
-                      out=o, final_state_out=fs, stream=stream)
+                      out=o_, final_state_out=fs_, stream=s_)
 
+    def step(_i=0):
+        call(dd, o, fs, stream)
+
+    cold = cold_call(step, stream, dev)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     if gdn.get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
+        raise RuntimeError(f"device error during the {name} warm-up")
+    with ClockSampler(dev.index) as clk:
+        ms, per = timed_launches(step, steps, stream, dev, world)
     if gdn.get_device_error() != 0:
-        raise RuntimeError("device error during the timed region")
-    ms = ev0.elapsed_time(ev1) / args.steps
+        raise RuntimeError(f"device error during the timed {name} region")
     ms_max = max_over_ranks(ms, world, dev)
     value = aggregate_throughput(T, world, ms_max / 1e3)
 
     bytes_, flops = prefill_algorithmic(w)
     gbs = bytes_ / (ms / 1e3) / 1e9
     tfs = flops / (ms / 1e3) / 1e12
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4),
-                "traffic": args.traffic if args.traffic is not None else recorded_traffic(),
-                "peak_source": peak_kind, "algorithmic_bytes_per_launch": int(bytes_),
+                "traffic": (args.traffic if args.traffic is not None else recorded_traffic()) if main else None,
+                "peak_source": PEAK_SOURCE, "algorithmic_bytes_per_launch": int(bytes_),
+                "arithmetic_intensity_flop_per_byte": round(flops / bytes_, 1),
+                "ridge_flop_per_byte": round(ridge, 1),
+                "frac_of_min_roof": round(tfs * 1e12 / min(peaks["bf16_tflops"] * 1e12,
+                                                           flops / bytes_ * peaks["hbm_gbs"] * 1e9), 4),
                 "tensor": {"achieved_tflops": round(tfs, 1), "peak_tflops": peaks["bf16_tflops"],
                            "frac": round(tfs / peaks["bf16_tflops"], 4),
                            "algorithmic_flops_per_launch": flops}}
 
-    # end to end through the C ABI with host buffers: H2D of the step's inputs
-    # from pinned memory, the call, D2H of the outputs, all inside the timed region
     e2e = None
     if not args.skip_e2e:
-        host = {k: w[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
-        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        fs_h = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = o.numel() * o.element_size() + fs.numel() * fs.element_size()
-
-        def e2e_step():
-            for key, t in host.items():
-                dd[key].copy_(t, non_blocking=True)
-            step()
-            o_h.copy_(o, non_blocking=True)
-            fs_h.copy_(fs, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        n_e2e = max(2, min(args.steps, 10))
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, dev)
-        e2e = {"value": aggregate_throughput(T, world, e2e_s), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-
-    decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
-    epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o)
-    prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
-    backward = None if args.skip_backward else run_backward(args, dev, peaks, world, w, dd)
-    kda = None if args.skip_kda else run_kda(args, dev, peaks, world, w, dd)
+        keys = [k for k in ("q", "k", "v", "g", "beta", "h0") if w.get(k) is not None]
+        host_in = {k: w[k].contiguous().pin_memory() for k in keys}
+        dev_in = [{k: dd[k] for k in keys}, {k: torch.empty_like(dd[k]) for k in keys}]
+        dev_out = [{"o": o, "fs": fs}, {"o": torch.empty_like(o), "fs": torch.empty_like(fs)}]
+        host_out = {"o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                    "fs": torch.empty(fs.shape, dtype=fs.dtype).pin_memory()}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        n_e2e = max(3, min(steps, 10 if T <= 20000 else 4))
+        sec = e2e_pipelined(host_in, dev_in, lambda i, o_, s_: call(i, o_["o"], o_["fs"], s_), dev_out, host_out,
+                            n_e2e, dev, world)
+        if gdn.get_device_error() != 0:
+            raise RuntimeError(f"device error in the {name} end-to-end run")
+        e2e = {"value": aggregate_throughput(T, world, sec), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "how": "C ABI call on host buffers: pinned H2D of the step's inputs, the call, D2H of o and the "
+                      "final states, every step; copies of one step overlap the previous step's call "
+                      "(three streams, double-buffered device tensors)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu_baseline:
-        tok_s, cores, sample = oracle_sample(w, target_s=args.cpu_seconds)
-        cpu = {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = oracle_baseline(w, cpu_seconds)
 
-    seq = f"T={T // N}" if w["cu_seqlens"] is None else f"lengths U{{{min(lengths)}..{max(lengths)}}}"
+    cfg = workload_config(name, w, world)
     return {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: B={N}, {seq}, H_qk={w['h_qk']}, H_v={w['h_v']}, "
-                               f"d_k=d_v={w['d_k']}, chunk 64, bf16 q/k/v/o, fp32 g/beta/state",
-                   "global_batch": N * world, "seq_len": T // N, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (126 MB) every step; no flush"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
-        "clocks": clk.summary(), "decode": decode, "epilogue": epilogue, "prologue": prologue,
-        "backward": backward, "kda": kda,
+        "value": value, "unit": "tokens/s", "ms_per_step": ms_max, "steps": steps, "config": cfg,
+        "workload": cfg["workload"], "tokens": T,
+        "timing": dict(median_ci95(per), unit="ms per launch", mean=ms), "cold_first_call": cold,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
+        "clocks": clk.summary(),
     }
+
+
+def run_ours(args, world, rank, local):
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    main = run_prefill_leg(args, args.workload, dev, peaks, world, rank, args.steps, args.cpu_seconds, main=True)
+    legs = {}
+    if not args.skip_long_varlen and args.workload == "prefill":
+        for name in ("long", "varlen"):
+            legs[name] = run_prefill_leg(args, name, dev, peaks, world, rank, max(3, min(args.steps, 10)),
+                                         args.cpu_seconds)
+            torch.cuda.empty_cache()
+    o_shape = (main["tokens"], 32, 128)
+    decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
+    epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o_shape)
+    w = gdn_inputs.make_workload("prefill", seed=args.seed + rank)
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
+    backward = None if args.skip_backward else run_backward(args, dev, peaks, world, w, dd)
+    kda = None if args.skip_kda else run_kda(args, dev, peaks, world, w, dd)
+    launches = main["gpu_launches"]
+    return {
+        "metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": main["config"],
+        "roofline": main["roofline"], "cpu_baseline": main["cpu_baseline"], "e2e": main["e2e"],
+        "gpu_launches": launches, "clocks": main["clocks"], "timing": main["timing"],
+        "cold_first_call": main["cold_first_call"],
+        "long": legs.get("long"), "varlen": legs.get("varlen"),
+        "decode": decode, "epilogue": epilogue, "prologue": prologue, "backward": backward, "kda": kda,
+    }
+
+
+def _timing(per, mean_ms, unit_scale=1.0, unit="ms per launch"):
+    t = median_ci95([x * unit_scale for x in per])
+    t.update(unit=unit, mean=mean_ms * unit_scale)
+    return t
 
 
 def run_decode(args, dev, peaks, world):
@@ -350,66 +513,58 @@ def run_decode(args, dev, peaks, world):
     o = torch.empty(wl.num_seqs, wl.h_v, wl.d_v, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def run(n0, n1):
-        for t in range(n0, n1):
-            gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state,
-                            out=o, stream=stream)
+    def one(t):
+        gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state,
+                        out=o, stream=stream)
 
-    run(0, min(3, steps))
+    cold = cold_call(lambda: one(0), stream, dev)
+    for t in range(1, min(4, steps)):
+        one(t)
     torch.cuda.synchronize(dev)
     state.copy_(dd["state"])
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        run(0, steps)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
+        ms, per = timed_launches(one, steps, stream, dev, world)
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error in decode")
-    us = ev0.elapsed_time(ev1) * 1e3 / steps
-    us = max_over_ranks(us, world, dev)
+    us = max_over_ranks(ms * 1e3, world, dev)
     b = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v)
     gbs = b / (us / 1e6) / 1e9
     return {"workload": f"decode: {wl.num_seqs} sequences x H_v={wl.h_v} (H_qk={wl.h_qk}) x 128x128 fp32 "
                         f"states (512 MiB, > L2), bf16 token inputs and output, {steps} in-place steps",
             "us_per_step": us, "steps_per_s": 1e6 / us, "tokens_per_s": wl.num_seqs * 1e6 / us * world,
             "GB_per_s": gbs * world, "gpu_launches": steps, "clocks": clk.summary(),
+            "timing": _timing(per, ms, 1e3, "us per step"), "cold_first_call": cold,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
 
 
-def run_epilogue(args, dev, peaks, world, o):
+def run_epilogue(args, dev, peaks, world, o_shape):
     """The GDN output epilogue (zero-centred RMSNorm x sigmoid gate): standalone
-    on the prefill output, and fused into the decode step."""
+    on a tensor shaped like the prefill output, and fused into the decode step."""
     import gated_deltanet_recurrence_05_b300 as gdn
     gen = torch.Generator().manual_seed(args.seed + 99)
+    o = torch.randn(o_shape, generator=gen).to(torch.bfloat16).to(dev)
     z = torch.randn(o.shape, generator=gen).to(torch.bfloat16).to(dev)
     wn = (torch.randn(o.shape[-1], generator=gen) * 0.2).to(dev)
     y = torch.empty_like(o)
     stream = torch.cuda.current_stream(dev)
     reps = max(3, args.steps)
+    launch = lambda i=0: gdn.gated_rmsnorm(o, z, wn, out=y, stream=stream)
+    cold = cold_call(launch, stream, dev)
     for _ in range(3):
-        gdn.gated_rmsnorm(o, z, wn, out=y, stream=stream)
-    torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    ev0.record(stream)
-    for _ in range(reps):
-        gdn.gated_rmsnorm(o, z, wn, out=y, stream=stream)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+        launch()
+    ms, per = timed_launches(launch, reps, stream, dev, world)
+    us = max_over_ranks(ms * 1e3, world, dev)
     b = 3 * o.numel() * o.element_size() + wn.numel() * 4
     gbs = b / (us / 1e6) / 1e9
-    out = {"standalone": {"workload": f"gated RMSNorm on the prefill output {list(o.shape)} bf16 (gate bf16, "
-                                      f"weight fp32), > L2 every launch",
+    out = {"standalone": {"workload": f"gated RMSNorm on a bf16 tensor shaped like the prefill output {list(o.shape)} "
+                                      f"(gate bf16, weight fp32), > L2 every launch",
                           "us_per_launch": us, "GB_per_s": gbs * world, "gpu_launches": reps,
+                          "timing": _timing(per, ms, 1e3, "us per launch"), "cold_first_call": cold,
                           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                                        "algorithmic_bytes_per_launch": int(b)}}}
+    del o, z, y
     if not args.skip_decode:
         wl = gdn_inputs.WORKLOADS["decode"]
         steps = min(args.decode_steps, 200)
@@ -420,26 +575,23 @@ def run_epilogue(args, dev, peaks, world, o):
         zd = torch.randn(steps, wl.num_seqs, wl.h_v, wl.d_v, generator=gen).to(torch.bfloat16).to(dev)
         wd = (torch.randn(wl.d_v, generator=gen) * 0.2).to(dev)
 
-        def run(n0, n1):
-            for t in range(n0, n1):
-                gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state, out=od,
-                                gate=zd[t], norm_weight=wd, stream=stream)
+        def one(t):
+            gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state, out=od,
+                            gate=zd[t], norm_weight=wd, stream=stream)
 
-        run(0, min(3, steps))
+        for t in range(min(3, steps)):
+            one(t)
         torch.cuda.synchronize(dev)
         state.copy_(dd["state"])
-        barrier(world)
-        ev0.record(stream)
-        run(0, steps)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
+        ms_d, per_d = timed_launches(one, steps, stream, dev, world)
         if gdn.get_device_error() != 0:
             raise RuntimeError("device error in the gated decode")
-        us_d = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / steps, world, dev)
+        us_d = max_over_ranks(ms_d * 1e3, world, dev)
         bd = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v) + zd[0].numel() * 2 + wd.numel() * 4
         gbd = bd / (us_d / 1e6) / 1e9
         out["fused_decode"] = {"workload": "the decode workload with the epilogue fused (gate bf16 per step)",
                                "us_per_step": us_d, "gpu_launches": steps,
+                               "timing": _timing(per_d, ms_d, 1e3, "us per step"),
                                "roofline": {"bound": "hbm", "achieved": round(gbd, 1), "peak": peaks["hbm_gbs"],
                                             "unit": "GB/s", "frac": round(gbd / peaks["hbm_gbs"], 4),
                                             "algorithmic_bytes_per_launch": int(bd)}}
@@ -460,31 +612,27 @@ def run_prologue(args, dev, peaks, world, w):
         wt = (torch.randn(C, 4, generator=gen) * 0.5).to(dev)
         bufs.append((x, wt, torch.empty_like(x), ng))
     stream = torch.cuda.current_stream(dev)
+    cu = w["cu_seqlens"].to(dev) if w["cu_seqlens"] is not None else None
 
-    def step():
+    def step(_i=0):
         for x, wt, y, ng in bufs:
-            gdn.short_conv(x, wt, cu_seqlens=w["cu_seqlens"].to(dev) if w["cu_seqlens"] is not None else None,
-                           num_seqs=N, norm_group=ng, out=y, stream=stream)
+            gdn.short_conv(x, wt, cu_seqlens=cu, num_seqs=N, norm_group=ng, out=y, stream=stream)
 
+    cold = cold_call(step, stream, dev)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
     reps = max(3, args.steps)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    ev0.record(stream)
-    for _ in range(reps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, per = timed_launches(step, reps, stream, dev, world)
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error in the prologue")
-    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+    us = max_over_ranks(ms * 1e3, world, dev)
     b = sum(2 * x.numel() * x.element_size() + wt.numel() * 4 for x, wt, _, _ in bufs)
     gbs = b / (us / 1e6) / 1e9
     return {"workload": f"short conv (K=4) + silu (+ L2 norm per head for q, k) on the q, k [{T}, "
                         f"{shapes[0][0]}] and v [{T}, {shapes[2][0]}] bf16 projections of the prefill workload",
             "us_per_step": us, "GB_per_s": gbs * world, "gpu_launches": 3 * reps,
+            "timing": _timing(per, ms, 1e3, "us per step (three launches)"), "cold_first_call": cold,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
 
@@ -522,20 +670,15 @@ def run_backward(args, dev, peaks, world, w, dd):
         gdn.chunk_bwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], do, dd["h0"], dht, cu,
                       num_seqs=None if cu is not None else N, out=outs, workspace=ws, stream=stream)
 
+    cold = cold_call(step, stream, dev)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
     reps = max(3, min(args.steps, 10))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    ev0.record(stream)
-    for _ in range(reps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms, per = timed_launches(lambda i: step(), reps, stream, dev, world)
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error in the backward")
-    us = max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+    us = max_over_ranks(ms * 1e3, world, dev)
     flops = backward_algorithmic(T, h_v, d_k, d_v)
     tfs = flops / (us / 1e6) / 1e12
 
@@ -555,6 +698,7 @@ def run_backward(args, dev, peaks, world, w, dd):
                         f"d=128, bf16 q/k/v/dO, fp32 g/beta/dS_T, fp32 gradients)",
             "us_per_step": us, "tokens_per_s": T * world / (us / 1e6),
             "gpu_launches": reps * (2 if h_v > h_qk else 1), "cpu_baseline": cpu,
+            "timing": _timing(per, ms, 1e3, "us per gradient step"), "cold_first_call": cold,
             "roofline": {"bound": "alu", "achieved": round(tfs, 2), "peak": round(SIMT_FP32_TFLOPS, 1),
                          "unit": "TFLOP/s", "frac": round(tfs / SIMT_FP32_TFLOPS, 4),
                          "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz",
@@ -580,23 +724,20 @@ def run_kda(args, dev, peaks, world, w, dd):
         gdn.kda_chunk_fwd(dd["q"], dd["k"], dd["v"], g, dd["beta"], dd["h0"], cu,
                           num_seqs=None if cu is not None else N, out=o, final_state_out=fs, stream=stream)
 
-    def timed(fn, reps):
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for i in range(reps):
-            fn(i)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
+    timings = {}
+
+    def timed(fn, reps, key):
+        ms, per = timed_launches(fn, reps, stream, dev, world)
         if gdn.get_device_error() != 0:
             raise RuntimeError("device error in KDA")
-        return max_over_ranks(ev0.elapsed_time(ev1) * 1e3 / reps, world, dev)
+        timings[key] = _timing(per, ms, 1e3, "us per launch")
+        return max_over_ranks(ms * 1e3, world, dev)
 
+    cold = cold_call(prefill, stream, dev)
     for _ in range(3):
         prefill()
     reps = max(3, min(args.steps, 10))
-    us_pf = timed(lambda i: prefill(), reps)
+    us_pf = timed(lambda i: prefill(), reps, "prefill")
     flops = 6.0 * d_k * d_v * T * h_v   # S^T (a o k), S^T (a o q), the decayed rank-1 update
     tfs = flops / (us_pf / 1e6) / 1e12
 
@@ -615,13 +756,14 @@ def run_kda(args, dev, peaks, world, w, dd):
     for i in range(3):
         dstep(i)
     state.copy_(tt["state"])
-    us_dec = timed(dstep, steps)
+    us_dec = timed(dstep, steps, "decode")
     # the decode step's bytes with g per key channel instead of one per head
     b = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v) + wl.num_seqs * wl.h_v * (wl.d_k - 1) * 4
     gbs = b / (us_dec / 1e6) / 1e9
     return {"prefill": {"workload": f"KDA prefill: the prefill workload (B={N}, T={T // N}) with per-channel "
                                     f"fp32 log-decays [T, {h_v}, {d_k}], bf16 o, fp32 final states",
                         "us_per_launch": us_pf, "tokens_per_s": T * world / (us_pf / 1e6), "gpu_launches": reps,
+                        "timing": timings["prefill"], "cold_first_call": cold,
                         "roofline": {"bound": "alu", "achieved": round(tfs, 2), "peak": round(SIMT_FP32_TFLOPS, 1),
                                      "unit": "TFLOP/s", "frac": round(tfs / SIMT_FP32_TFLOPS, 4),
                                      "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz",
@@ -629,6 +771,7 @@ def run_kda(args, dev, peaks, world, w, dd):
             "decode": {"workload": f"KDA decode: {wl.num_seqs} x {wl.h_v} states of 128x128 fp32, per-channel "
                                    f"decays, {steps} in-place steps",
                        "us_per_step": us_dec, "GB_per_s": gbs * world, "gpu_launches": steps,
+                       "timing": timings["decode"],
                        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                                     "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                                     "algorithmic_bytes_per_launch": int(b)}}}
@@ -649,12 +792,10 @@ def run_reference(args, world, rank):
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": T / value * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: B={N}, T={T // N}, H_qk={w['h_qk']}, H_v={w['h_v']}, "
-                                   f"d_k=d_v={w['d_k']}", "global_batch": N, "seq_len": T // N,
-                       "parallelism": "host cores"},
+            "config": workload_config(args.workload, w, world),
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "per_step": per_step},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -677,6 +818,7 @@ def main(argv=None):
     ap.add_argument("--skip-backward", action="store_true", help="skip the gradient line")
     ap.add_argument("--skip-kda", action="store_true", help="skip the per-channel-decay (KDA) lines")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-long-varlen", action="store_true", help="skip the long and varlen prefill lines")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup(args)

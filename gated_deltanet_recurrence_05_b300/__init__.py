@@ -26,11 +26,14 @@ from typing import Optional
 import torch
 
 __all__ = ["chunk_fwd", "decode_step", "plan_seq_order", "get_device_error", "lib",
-           "GdnError", "LIB_PATH", "F32", "BF16", "FLAG_FORCE_SIMT"]
+           "GdnError", "LIB_PATH", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_TEST_WAIT_TIMEOUT",
+           "DEVERR_SEQLENS", "DEVERR_TIMEOUT", "DEVERR_RANGE"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
+FLAG_TEST_WAIT_TIMEOUT = 2   # failure-path tests only (see include/gdn.h)
+DEVERR_SEQLENS, DEVERR_TIMEOUT, DEVERR_RANGE = 1, 2, 4
 _STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
            4: "GDN_ERR_TIMEOUT"}
 _lib = None
@@ -151,7 +154,7 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
               seq_order: Optional[torch.Tensor] = None, output_dtype: Optional[torch.dtype] = None,
               scale: float = 0.0, chunk_size: int = 0, output_final_state: bool = True,
               out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None,
-              force_simt: bool = False, stream=None):
+              force_simt: bool = False, test_wait_timeout: bool = False, stream=None):
     """Prefill of the recurrence over packed tokens (see include/gdn.h).
 
     q, k: [T, H_qk, d_k]; v: [T, H_v, d_v] (fp32 or bf16, one dtype); g, beta:
@@ -185,7 +188,8 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     st = lib().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
                              _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(fs), N, T, h_qk, h_v,
                              d_k, d_v, _code(q), _code(o), float(scale), int(chunk_size),
-                             FLAG_FORCE_SIMT if force_simt else 0, _stream(stream))
+                             (FLAG_FORCE_SIMT if force_simt else 0) |
+                             (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0), _stream(stream))
     _check("gdn_chunk_fwd", st)
     return o, fs
 
@@ -392,9 +396,13 @@ def plan_seq_order(cu_seqlens) -> torch.Tensor:
 
 
 def get_device_error(stream=None) -> int:
-    """Synchronise the stream and return (and clear) the GDN_DEVERR_* bits."""
+    """Synchronise the stream and return (and clear) the GDN_DEVERR_* bits.
+    (The C call's GDN_ERR_TIMEOUT status mirrors the DEVERR_TIMEOUT bit, which
+    is returned here like the other bits.)"""
     code = ctypes.c_uint32(0)
-    _check("gdn_get_device_error", lib().gdn_get_device_error(_stream(stream), ctypes.byref(code)))
+    st = lib().gdn_get_device_error(_stream(stream), ctypes.byref(code))
+    if st != 4:
+        _check("gdn_get_device_error", st)
     return int(code.value)
 
 

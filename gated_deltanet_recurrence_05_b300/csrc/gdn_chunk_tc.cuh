@@ -36,7 +36,11 @@
 // computed operands (S, Delta, T, W, P and the decay-scaled Q and Delta) are
 // rounded, at 2^-11 instead of bf16's 2^-8. Decay-scaled values that fall
 // below the fp16 range contribute less than 1e-7 of the largest terms. The
-// path therefore assumes |v| and |S| stay well below 6e4 (the fp16 range).
+// path therefore needs |v|, |S| and the errors Delta to stay below 65504 (the
+// fp16 range). A value beyond it becomes an infinity in the products and
+// leaves a non-finite fp32 state behind; every unit checks its final state
+// and records GDN_DEVERR_RANGE, so such inputs are reported, not silently
+// wrong (the fp32 CUDA-core kernel serves them).
 //
 // Warp roles (512 threads) are listed where they branch (chunk_tc_kernel).
 // One group of four prep warps builds T for every chunk (A/P pass, then the
@@ -45,7 +49,11 @@
 // purpose (rolled issue and conversion loops, one copy of each step): with 16
 // warps running different code the instruction cache was the first
 // bottleneck. All waits are bounded (a timeout raises an abort flag, records
-// GDN_DEVERR_TIMEOUT and every role unwinds); TMEM is always freed.
+// GDN_DEVERR_TIMEOUT and every role unwinds). On the way out nothing is left
+// in flight: the TMA producer waits for the last load of each ring stage it
+// filled, both MMA issuers commit a final barrier (B_DONE) that completes
+// only when every product they issued has finished, and TMEM is freed after
+// that barrier.
 #pragma once
 
 #include <cudaTypedefs.h>
@@ -63,6 +71,8 @@ struct TcArgs {
     int num_seqs; long long total; long long eq_len;
     int h_qk, h_v, grp;
     float scale;
+    uint32_t max_polls;    // poll limit of every mbarrier wait
+    int withhold_chunk;    // test of the failure path: the g/beta arrival of this chunk is never made (-1: none)
 };
 
 namespace tck {
@@ -401,7 +411,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     auto kq_tile = [&](int n) { return sm + OFF_KQ + (uint32_t)(n % KQ_STAGES) * KQ_BYTES; };
     auto v_tile = [&](int n) { return sm + OFF_V + (uint32_t)(n % V_STAGES) * V_BYTES; };
     auto gb_slot = [&](int n) { return reinterpret_cast<float*>(sm + OFF_GB + (uint32_t)(n % GB_SLOTS) * GB_SLOT_BYTES); };
-    auto WAIT = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, abort_flag); };
+    const uint32_t max_polls = p.max_polls;
+    auto WAIT = [&](int b, uint32_t parity) { return mbar_wait(&bars[b], parity, abort_flag, max_polls); };
     // warp-uniform wait (every lane polls; the warp proceeds only if all saw it)
     auto WAITW = [&](int b, uint32_t parity) { return __all_sync(0xffffffffu, WAIT(b, parity)) != 0; };
 
@@ -606,7 +617,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             gb[GB_QSC + r1] = r1 < L ? p.scale * e1 : 0.f;
             if (lane == 0) gb[GB_GC] = ex2(GL);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[B_GB_FULL + slot]);
+            // (a failure-path test withholds one arrival: every wait on it runs out)
+            if (lane == 0 && n != p.withhold_chunk) mbar_arrive(&bars[B_GB_FULL + slot]);
             if (lane == 0) GDN_TRACE_AT(41, n);
         }
     } else if (warp < 8) {
@@ -871,14 +883,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (n + 2 < nc && !convert(n + 2)) break;
             if (n >= 0 && ws == 0 && lane == 0) GDN_TRACE_AT(14, n);
         }
-        if (p.hT && !*abort_flag) {
-            float* hp = p.hT + sbase + (size_t)(64 * hf) * D + j;
+        if (!*abort_flag) {
+            // fp16 range: a value beyond the range of the fp16 operands (v, the
+            // state or a chunk's errors above 65504) became an infinity in a
+            // product and has left a non-finite value in the fp32 state, where
+            // it stays (decay keeps infinities, sums keep NaNs)
+            bool finite = true;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
+            for (int c = 0; c < 64; ++c) finite = finite && (fabsf(S[c]) < INFINITY);
+            if (__any_sync(0xffffffffu, !finite) && lane == 0) set_device_error(4u);
+            if (p.hT) {
+                float* hp = p.hT + sbase + (size_t)(64 * hf) * D + j;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
+            }
         }
     }
 
-    // ---- teardown: every product finished, then free TMEM
+    // ---- teardown (also after an abort): the producer has drained its TMA
+    //      loads; B_DONE completes when every MMA of both issuers is done;
+    //      only then is TMEM freed
     __syncthreads();
     if (warp == 1) {
         mbar_wait(&bars[B_DONE], 0, nullptr, 10000u);

@@ -404,7 +404,7 @@ gdn_status gdn_get_device_error(void* stream, uint32_t* code) {
     if (cudaMemcpyFromSymbol(&v, gdn::g_device_error, sizeof v) != cudaSuccess) return GDN_ERR_CUDA;
     if (cudaMemcpyToSymbol(gdn::g_device_error, &zero, sizeof zero) != cudaSuccess) return GDN_ERR_CUDA;
     *code = v;
-    return GDN_OK;
+    return (v & GDN_DEVERR_TIMEOUT) ? GDN_ERR_TIMEOUT : GDN_OK;
 }
 
 gdn_status gdn_decode_step_gated(const void* q, const void* k, const void* v, const float* g,
@@ -520,7 +520,7 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
         return GDN_ERR_INVALID_ARG;
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
     if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDN_ERR_INVALID_ARG;
-    if (flags & ~GDN_FLAG_FORCE_SIMT) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT)) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
@@ -544,6 +544,9 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
         a.cu = cu_seqlens; a.order = seq_order; a.o = o; a.hT = final_state;
         a.num_seqs = num_seqs; a.total = total_tokens; a.eq_len = eq_len;
         a.h_qk = h_qk; a.h_v = h_v; a.grp = h_v / h_qk; a.scale = scale;
+        const bool stall = (flags & GDN_FLAG_TEST_WAIT_TIMEOUT) != 0;
+        a.max_polls = stall ? (1u << 12) : (1u << 17);
+        a.withhold_chunk = stall ? 1 : -1;
         return gdn::launch_tc(a, bf_out, s);
     }
 

@@ -61,14 +61,32 @@ enum { GDN_F32 = 0, GDN_BF16 = 1 };
 
 /* Flags for gdn_chunk_fwd. */
 enum {
-    GDN_FLAG_FORCE_SIMT = 1    /* use the fp32 CUDA-core chunk kernel even where
-                                  the tensor-core kernel applies (cross-checks) */
+    GDN_FLAG_FORCE_SIMT = 1,   /* use the fp32 CUDA-core chunk kernel even where
+                                  the tensor-core kernel applies (cross-checks,
+                                  and inputs beyond the fp16 range: see
+                                  GDN_DEVERR_RANGE) */
+    GDN_FLAG_TEST_WAIT_TIMEOUT = 2
+                               /* for tests of the failure path only: the
+                                  tensor-core kernel withholds one internal
+                                  arrival (chunk 1 of every unit) and shortens
+                                  its wait limit to 4096 polls, so that its
+                                  waits run out; every role unwinds, drains its
+                                  copies and products and frees TMEM, and
+                                  GDN_DEVERR_TIMEOUT is recorded. o and the
+                                  final states are undefined after such a call;
+                                  the stream stays usable. No effect on the
+                                  CUDA-core kernel. */
 };
 
 /* Device error codes (bit set) returned by gdn_get_device_error. */
 enum {
     GDN_DEVERR_SEQLENS = 1,    /* cu_seqlens / seq_order entry out of range     */
-    GDN_DEVERR_TIMEOUT = 2     /* an mbarrier wait exceeded its iteration limit */
+    GDN_DEVERR_TIMEOUT = 2,    /* an mbarrier wait exceeded its iteration limit */
+    GDN_DEVERR_RANGE = 4       /* the tensor-core prefill met a value beyond the
+                                  range of its fp16 products (|v|, |S| or a
+                                  chunk's errors above 65504) and left a
+                                  non-finite final state: rerun that call with
+                                  GDN_FLAG_FORCE_SIMT (fp32 throughout)       */
 };
 
 /*
@@ -95,6 +113,9 @@ enum {
  * Kernels: bf16 inputs with d_k = d_v = 128 run the tcgen05/TMEM kernel with
  * TMA-fed tiles and the fp32 state kept on chip across chunks; everything else
  * (fp32 inputs, other head sizes up to 128) runs the fp32 CUDA-core kernel.
+ * The tensor-core kernel multiplies fp16 operands (fp32 accumulation): it
+ * needs |v|, the state and each chunk's errors below 65504, checks every
+ * unit's final state and records GDN_DEVERR_RANGE when that failed.
  * Returns GDN_ERR_INVALID_ARG for null/misaligned pointers, H_v % H_qk != 0,
  * N < 0, T_total < 0, T_total % N != 0 without cu_seqlens, or bad codes;
  * GDN_ERR_UNSUPPORTED for d_k or d_v outside 1..128.
@@ -388,7 +409,10 @@ gdn_status gdn_plan_seq_order(const int32_t* cu_seqlens_host, int32_t num_seqs,
 /*
  * gdn_get_device_error -- synchronises `stream`, then returns in *code the
  * GDN_DEVERR_* bits recorded by kernels of this library on the current
- * device since the last call, and clears them.
+ * device since the last call, and clears them. The status is GDN_ERR_TIMEOUT
+ * when the bits include GDN_DEVERR_TIMEOUT (a kernel gave up on a wait and
+ * unwound), GDN_ERR_CUDA when the synchronisation or the read failed, and
+ * GDN_OK otherwise (other bits are reported in *code only).
  */
 gdn_status gdn_get_device_error(void* stream, uint32_t* code);
 

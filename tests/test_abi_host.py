@@ -92,6 +92,7 @@ def _fwd(L, **kw):
     (dict(do=2), INVALID),
     (dict(chunk=48), INVALID),
     (dict(flags=8), INVALID),
+    (dict(flags=2 | 16), INVALID),               # only documented flag bits
     (dict(d_k=256), UNSUPPORTED),
     (dict(d_v=129), UNSUPPORTED),
     (dict(N=0, T=0), OK),                        # nothing to do

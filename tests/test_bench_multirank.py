@@ -67,3 +67,22 @@ def test_traffic_summary_is_tied_to_kernel_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic() == 123.0
     f.write_text("kernel_sha256: 0000\ndram_bytes_per_launch: 123\n")
     assert bench.recorded_traffic() is None
+
+
+def test_median_ci95_order_statistics():
+    """The confidence interval of the median is the narrowest symmetric pair of
+    order statistics that covers the median with probability >= 0.95 under
+    the binomial law (n = 20: the 6th and 15th values, the textbook pair)."""
+    import math
+    r = bench.median_ci95(list(range(1, 21)))
+    assert r["median"] == 10.5 and r["ci95"] == [6.0, 15.0] and r["n"] == 20
+    for n in (5, 6, 10, 50, 101):
+        xs = list(range(n))
+        lo, hi = bench.median_ci95(xs)["ci95"]
+        j, k = int(lo), int(hi)
+        cover = sum(math.comb(n, i) for i in range(j + 1, k + 1)) / 2.0 ** n
+        assert cover >= 0.95 or (j, k) == (0, n - 1)   # n < 6: the whole range is the widest there is
+        if j + 1 <= n - 2 - j:  # one order statistic narrower on each side would not cover
+            narrower = sum(math.comb(n, i) for i in range(j + 2, k)) / 2.0 ** n
+            assert narrower < 0.95
+    assert bench.median_ci95([3.0])["ci95"] == [3.0, 3.0]
