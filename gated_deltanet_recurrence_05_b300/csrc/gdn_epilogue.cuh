@@ -8,8 +8,8 @@
 // gate multiplies its result, w is the zero-centred per-feature weight shared
 // by all heads, and z (= x W_g) is the caller's.
 //
-// Standalone kernel (after the prefill, or on any [rows, d] tensor): one warp
-// per row, one warp-shuffle reduction.
+// Standalone kernels (after the prefill, or on any [rows, d] tensor): a
+// half-warp per row of 128 (16-byte accesses), one warp per row otherwise.
 // It moves 3 values per feature (o and z in, y out) and is HBM-bound.
 #pragma once
 
@@ -88,68 +88,85 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
 }
 __device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-// d = 128 with 16-byte aligned bases: lane l owns features 4l .. 4l + 3 of a
-// row (one vector load of x and of z), and each warp keeps R = 4 rows in
-// flight so that enough bytes are outstanding per SM to reach HBM bandwidth.
-// Raw 4-element vectors (kept packed until used: fewer registers, more rows
-// in flight per SM).
-template <typename T> struct Vec4;
-template <> struct Vec4<__nv_bfloat16> { using type = uint2; };
-template <> struct Vec4<float> { using type = float4; };
-template <typename T>
-__device__ __forceinline__ typename Vec4<T>::type load_raw4(const T* p) {
-    return *reinterpret_cast<const typename Vec4<T>::type*>(p);
+// Eight consecutive elements as raw 32-bit words (one 16-byte load of bf16,
+// two of fp32) and their fp32 values.
+template <typename T> struct Raw8 { uint32_t u[4 * (int)sizeof(T) / 2]; };
+template <typename T> __device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
+    Raw8<T> r;
+#pragma unroll
+    for (int i = 0; i < 2 * (int)sizeof(T); i += 4) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(p) + i));
+        r.u[i] = a.x; r.u[i + 1] = a.y; r.u[i + 2] = a.z; r.u[i + 3] = a.w;
+    }
+    return r;
 }
-__device__ __forceinline__ float4 unpack4(uint2 u) {
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+__device__ __forceinline__ float raw8_val(const Raw8<__nv_bfloat16>& r, int j) {
+    return __uint_as_float((j & 1) ? (r.u[j >> 1] & 0xffff0000u) : (r.u[j >> 1] << 16));
 }
-__device__ __forceinline__ float4 unpack4(float4 f) { return f; }
+__device__ __forceinline__ float raw8_val(const Raw8<float>& r, int j) { return __uint_as_float(r.u[j]); }
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
+        w[h] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    __stcs(reinterpret_cast<uint4*>(p), u);
+}
+__device__ __forceinline__ void store8(float* p, const float* v) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(v[4], v[5], v[6], v[7]));
+}
 
-// d = 128 with 16-byte aligned bases: lane l owns features 4l .. 4l + 3 of a
-// row (one vector load of x and of z), and each warp keeps R = 4 rows in
-// flight (raw vectors until used) so that enough bytes are outstanding per SM
-// to reach HBM bandwidth.
+// d = 128 with 16-byte aligned bases: a half-warp per row, lane l owning
+// features 8 (l % 16) .. + 7 (one 16-byte load of x and of z for bf16), the
+// sum of squares reduced in four shuffles inside the half-warp. Each warp
+// takes R row pairs per iteration and issues all their loads before any
+// arithmetic, with streaming (evict-first) loads and stores: every byte is
+// touched once.
 template <typename TX, typename TZ, typename TY>
 __global__ void __launch_bounds__(256)
 gated_rmsnorm_d128_kernel(const TX* x, const TZ* __restrict__ z, const float* __restrict__ w, TY* y,
                           long long rows, float eps) {
-    constexpr int D = 128, R = 4;
-    const int lane = threadIdx.x & 31;
-    float4 ws = w ? *reinterpret_cast<const float4*>(w + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    ws.x += 1.0f; ws.y += 1.0f; ws.z += 1.0f; ws.w += 1.0f;  // zero-centred weight -> scale
+    constexpr int D = 128, R = 2;
+    const int lane = threadIdx.x & 31, hl = lane & 15, half = lane >> 4;
+    float ws[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ws[j] = 1.0f + (w ? w[8 * hl + j] : 0.f);  // zero-centred weight -> scale
     const long long warps = (long long)gridDim.x * 8;
-    for (long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * R; r0 < rows; r0 += warps * R) {
-        typename Vec4<TX>::type xr[R];
-        typename Vec4<TZ>::type zr[R];
+    for (long long r0 = ((long long)blockIdx.x * 8 + (threadIdx.x >> 5)) * (2 * R); r0 < rows;
+         r0 += warps * (2 * R)) {
+        Raw8<TX> xr[R];
+        Raw8<TZ> zr[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            const long long row = r0 + i < rows ? r0 + i : rows - 1;  // tail rows repeat the last row
-            xr[i] = load_raw4(x + row * D + 4 * lane);
-            zr[i] = load_raw4(z + row * D + 4 * lane);
+            long long row = r0 + 2 * i + half;
+            row = row < rows ? row : rows - 1;  // tail rows repeat the last row (not stored)
+            xr[i] = load_raw8(x + row * D + 8 * hl);
+            zr[i] = load_raw8(z + row * D + 8 * hl);
         }
         float ss[R];
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            const float4 v = unpack4(xr[i]);
-            ss[i] = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            float a = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaf(raw8_val(xr[i], j), raw8_val(xr[i], j), a);
+            ss[i] = a;
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
+        for (int off = 8; off > 0; off >>= 1) {
 #pragma unroll
             for (int i = 0; i < R; ++i) ss[i] += __shfl_xor_sync(0xffffffffu, ss[i], off);
         }
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-            if (r0 + i >= rows) break;
+            const long long row = r0 + 2 * i + half;
             const float rinv = rsqrtf(fmaf(ss[i], 1.0f / D, eps));
-            const float4 v = unpack4(xr[i]), g = unpack4(zr[i]);
-            float4 o;
-            o.x = v.x * (rinv * ws.x) * sigmoid_f(g.x);
-            o.y = v.y * (rinv * ws.y) * sigmoid_f(g.y);
-            o.z = v.z * (rinv * ws.z) * sigmoid_f(g.z);
-            o.w = v.w * (rinv * ws.w) * sigmoid_f(g.w);
-            store4(y + (r0 + i) * D + 4 * lane, o);
+            float o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) o[j] = raw8_val(xr[i], j) * (rinv * ws[j]) * sigmoid_f(raw8_val(zr[i], j));
+            if (row < rows) store8(y + row * D + 8 * hl, o);
         }
     }
 }

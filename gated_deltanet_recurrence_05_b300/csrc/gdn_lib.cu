@@ -117,7 +117,7 @@ template <typename T, int K>
 gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32_t* cu, const float* st_in,
                              float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s) {
     const DevInfo di = dev_info();
-    const long long runs = (total + 31) / 32;  // 32 tokens per warp
+    const long long runs = (total + 7) / 8;  // tiles of 8 tokens, one per warp
     // 8 channels per lane when the channels and the head size allow it
     const bool v8 = C % 256 == 0 && (ng == 0 || ng >= 8);
     const int cblocks = v8 ? C / 256 : (C + 127) / 128;

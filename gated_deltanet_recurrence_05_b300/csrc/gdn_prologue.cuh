@@ -8,10 +8,10 @@
 // sequence's first tokens is the caller's conv state (its K-1 preceding
 // inputs, oldest first) or zero; the final state is the last K-1 inputs.
 //
-// One warp per (token, block of 128 channels): lane l owns channels
-// 128 b + 4 l .. + 3 (one vector load per tap), so a head of up to 128
-// channels is reduced inside the warp. Both kernels are HBM-bound: x is read
-// once from DRAM (the K taps of neighbouring tokens hit L1/L2) and y written
+// One warp per (tile of 8 tokens, block of 32 V channels): lane l owns V = 4
+// or 8 consecutive channels (one 8- or 16-byte load per row), so a head of up
+// to 32 V channels is reduced inside the warp. Both kernels are HBM-bound: x
+// is read once from DRAM (the K-1 halo rows of a tile hit L2) and y written
 // once.
 #pragma once
 
@@ -48,8 +48,19 @@ template <int V, typename T> __device__ __forceinline__ void loadVf(const T* p, 
     for (int h = 0; h < V / 4; ++h) load4f(p + 4 * h, v + 4 * h);
 }
 template <int V, typename T> __device__ __forceinline__ void storeVf(T* p, const float* v) {
+    if constexpr (V == 8 && sizeof(T) == 2) {  // eight bf16: one 16-byte store
+        uint4 u;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
-    for (int h = 0; h < V / 4; ++h) store4f(p + 4 * h, v + 4 * h);
+        for (int h = 0; h < 4; ++h) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
+            w[h] = *reinterpret_cast<uint32_t*>(&b);
+        }
+        *reinterpret_cast<uint4*>(p) = u;
+    } else {
+#pragma unroll
+        for (int h = 0; h < V / 4; ++h) store4f(p + 4 * h, v + 4 * h);
+    }
 }
 
 // silu, then the L2 norm over groups of `ng` channels (ng = 0: none; else a
@@ -71,7 +82,7 @@ __device__ __forceinline__ void silu_norm(float* s, int ng, float eps) {
 
 // Sequence of token t: cu == nullptr means num_seqs sequences of eq_len.
 __device__ __forceinline__ int seq_of_token(const int32_t* cu, int num_seqs, long long eq_len, long long t) {
-    if (cu == nullptr) return (int)(t / eq_len);
+    if (cu == nullptr) return (int)((uint32_t)t / (uint32_t)eq_len);  // token counts fit 31 bits
     int lo = 0, hi = num_seqs;  // cu[lo] <= t < cu[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -80,17 +91,53 @@ __device__ __forceinline__ int seq_of_token(const int32_t* cu, int num_seqs, lon
     return lo;
 }
 
-// Each warp filters a run of RUN consecutive tokens for one block of 32 V
-// channels (V per lane: 4, or 8 when C and the head size allow): the taps
-// slide through registers (one load and one store per token), the weights are
-// loaded once per run, and a run crossing into the next sequence restarts its
-// window from that sequence's state.
+// V consecutive elements of a row as raw 32-bit words (bf16 pairs or fp32),
+// kept packed in registers until a tap uses them.
+template <typename T, int V> struct RawRow {
+    static constexpr int W = V * (int)sizeof(T) / 4;
+    uint32_t u[W];
+};
+template <typename T, int V>
+__device__ __forceinline__ RawRow<T, V> load_row(const T* p) {
+    RawRow<T, V> r;
+    constexpr int W = RawRow<T, V>::W;  // 2 (8-byte load), 4 or 8 (one or two 16-byte loads)
+    if constexpr (W == 2) {
+        const uint2 a = *reinterpret_cast<const uint2*>(p);
+        r.u[0] = a.x; r.u[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; i += 4) {
+            const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint32_t*>(p) + i);
+            r.u[i] = a.x; r.u[i + 1] = a.y; r.u[i + 2] = a.z; r.u[i + 3] = a.w;
+        }
+    }
+    return r;
+}
+template <typename T, int V> __device__ __forceinline__ RawRow<T, V> zero_row() {
+    RawRow<T, V> r;
+#pragma unroll
+    for (int i = 0; i < RawRow<T, V>::W; ++i) r.u[i] = 0u;
+    return r;
+}
+__device__ __forceinline__ float raw_val(const uint32_t* u, int j, const __nv_bfloat16*) {
+    return __uint_as_float((j & 1) ? (u[j >> 1] & 0xffff0000u) : (u[j >> 1] << 16));
+}
+__device__ __forceinline__ float raw_val(const uint32_t* u, int j, const float*) { return __uint_as_float(u[j]); }
+
+// Tiled filter: each warp takes a tile of TT consecutive tokens for one block
+// of 32 V channels (V per lane, 16-byte loads). It loads the tile's rows and
+// the K-1 rows before it in one batch (all loads in flight together; the
+// halo rows are re-read from L2 by the neighbouring tile), then evaluates the
+// tokens one by one from registers: the taps of a token that fall before its
+// sequence's first token come from the caller's conv state (or are zero), and
+// a tile may span several sequences. The warp that holds a sequence's last
+// token writes that sequence's final conv state.
 template <typename T, int K, int V>
 __global__ void __launch_bounds__(256)
 short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
                   const int32_t* __restrict__ cu, const float* __restrict__ st_in, float* __restrict__ st_out,
                   int num_seqs, long long total, long long eq_len, int C, int ng, float eps) {
-    constexpr int RUN = 32;
+    constexpr int TT = 8, H = K - 1, NR = TT + H;
     const int lane = threadIdx.x & 31;
     const int c = (int)blockIdx.y * (32 * V) + V * lane;
     const bool live = c < C;  // C % V == 0: a lane's V channels are all in or all out
@@ -99,85 +146,103 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
     for (int j = 0; j < V; ++j)
 #pragma unroll
         for (int i = 0; i < K; ++i) wv[j][i] = live ? w[(size_t)(c + j) * K + i] : 0.f;
-    const long long runs = (total + RUN - 1) / RUN;
-    for (long long rr = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); rr < runs; rr += (long long)gridDim.x * 8) {
-        const long long ta = rr * RUN, tb = ta + RUN < total ? ta + RUN : total;
-        int n = seq_of_token(cu, num_seqs, eq_len, ta);
+    const long long tiles = (total + TT - 1) / TT;
+    for (long long tile = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); tile < tiles;
+         tile += (long long)gridDim.x * 8) {
+        const long long tb = tile * TT;
+        const int nt = (int)(total - tb < TT ? total - tb : TT);
+        // row r holds the input of token tb - H + r
+        RawRow<T, V> rows[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const long long p = tb - H + r;
+            rows[r] = (live && p >= 0 && r < H + nt) ? load_row<T, V>(x + p * C + c) : zero_row<T, V>();
+        }
+        int n = seq_of_token(cu, num_seqs, eq_len, tb);
         long long t0 = cu ? cu[n] : (long long)n * eq_len;
         long long t1 = cu ? cu[n + 1] : t0 + eq_len;
-        float win[K][V];  // win[i] = input at t - (K-1) + i
-        bool bad = false;
-        auto restart = [&](long long t) {  // window for token t of sequence n
+        bool bad = tb < t0 || tb >= t1 || t0 < 0 || t1 > total;
+        if (!bad && nt == TT && tb - H >= t0 && tb + TT <= t1) {
+            // Common case: the tile and its halo lie inside one sequence. Straight-line
+            // code: each row is widened to fp32 once and slides through the window.
+            float win[K][V];
 #pragma unroll
-            for (int i = 0; i < K - 1; ++i) {
-                const long long p = t - (K - 1) + i;
-                if (!live) {
+            for (int i = 0; i < H; ++i)
 #pragma unroll
-                    for (int j = 0; j < V; ++j) win[i][j] = 0.f;
-                } else if (p >= t0) {
-                    loadVf<V>(x + p * C + c, win[i]);
-                } else if (st_in) {  // the caller's past: entry p - t0 + K - 1
-                    const float* sp = st_in + ((size_t)n * C + c) * (K - 1) + (p - t0 + K - 1);
+                for (int j = 0; j < V; ++j) win[i][j] = raw_val(rows[i].u, j, x);
+            T* yp = y + tb * C + c;
 #pragma unroll
-                    for (int j = 0; j < V; ++j) win[i][j] = sp[j * (K - 1)];
-                } else {
+            for (int k = 0; k < TT; ++k) {
 #pragma unroll
-                    for (int j = 0; j < V; ++j) win[i][j] = 0.f;
-                }
-            }
-        };
-        if (ta < t0 || ta >= t1 || t0 < 0 || t1 > total) bad = true;
-        if (!bad) restart(ta);
-        // the run's inputs in batches of 8 tokens, loaded before they are used
-        constexpr int BATCH = V == 4 ? 8 : 4;
-        float xb[BATCH][V];
-        for (long long tq = ta; tq < tb && !bad; tq += BATCH) {
-#pragma unroll
-            for (int k = 0; k < BATCH; ++k) {
-                if (live && tq + k < tb) loadVf<V>(x + (tq + k) * C + c, xb[k]);
-                else {
-#pragma unroll
-                    for (int j = 0; j < V; ++j) xb[k][j] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < BATCH; ++k) {
-                const long long t = tq + k;
-                if (t >= tb || bad) break;
-                while (t >= t1) {  // next non-empty sequence (warp-uniform)
-                    ++n;
-                    if (n >= num_seqs) { bad = true; break; }
-                    t0 = cu ? cu[n] : (long long)n * eq_len;
-                    t1 = cu ? cu[n + 1] : t0 + eq_len;
-                    if (t0 != t || t1 > total) { bad = true; break; }
-                    if (t < t1) restart(t);
-                }
-                if (bad) break;
-#pragma unroll
-                for (int j = 0; j < V; ++j) win[K - 1][j] = xb[k][j];
+                for (int j = 0; j < V; ++j) win[H][j] = raw_val(rows[k + H].u, j, x);
                 float acc[V];
 #pragma unroll
                 for (int j = 0; j < V; ++j) {
-                    float a = 0.f;
+                    float a = wv[j][0] * win[0][j];
 #pragma unroll
-                    for (int i = 0; i < K; ++i) a = fmaf(wv[j][i], win[i][j], a);
+                    for (int i = 1; i < K; ++i) a = fmaf(wv[j][i], win[i][j], a);
                     acc[j] = a;
                 }
-                silu_norm<V>(acc, ng, eps);  // every lane takes part in the shuffles
-                if (live) {
-                    storeVf<V>(y + t * C + c, acc);
-                    if (st_out && t == t1 - 1) {  // the K-1 newest inputs become the state
-                        float* so = st_out + ((size_t)n * C + c) * (K - 1);
+                silu_norm<V>(acc, ng, eps);
+                if (live) storeVf<V>(yp, acc);
+                yp += C;
 #pragma unroll
-                        for (int i = 1; i < K; ++i)
-#pragma unroll
-                            for (int j = 0; j < V; ++j) so[j * (K - 1) + (i - 1)] = win[i][j];
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < K - 1; ++i)
+                for (int i = 0; i < H; ++i)
 #pragma unroll
                     for (int j = 0; j < V; ++j) win[i][j] = win[i + 1][j];
+            }
+            if (st_out && live && tb + TT == t1) {  // the tile ends the sequence: its H newest inputs
+                float* so = st_out + ((size_t)n * C + c) * H;
+#pragma unroll
+                for (int i = 0; i < H; ++i)
+#pragma unroll
+                    for (int j = 0; j < V; ++j) so[j * H + i] = win[i][j];
+            }
+            continue;
+        }
+        // input at position p of sequence n (p < t0: the caller's past, or zero)
+        auto past = [&](long long p, int j) -> float {
+            return st_in ? st_in[((size_t)n * C + c + j) * H + (p - t0 + H)] : 0.f;
+        };
+#pragma unroll
+        for (int k = 0; k < TT; ++k) {
+            if (k >= nt || bad) break;
+            const long long t = tb + k;
+            while (t >= t1) {  // the next non-empty sequence starts here (warp-uniform)
+                ++n;
+                if (n >= num_seqs) { bad = true; break; }
+                t0 = cu ? cu[n] : (long long)n * eq_len;
+                t1 = cu ? cu[n + 1] : t0 + eq_len;
+                if (t0 != t || t1 > total) { bad = true; break; }
+            }
+            if (bad) break;
+            float acc[V];
+#pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] = wv[j][K - 1] * raw_val(rows[k + H].u, j, x);
+#pragma unroll
+            for (int i = 0; i < H; ++i) {
+                const long long p = t - H + i;
+                if (p >= t0) {
+#pragma unroll
+                    for (int j = 0; j < V; ++j) acc[j] = fmaf(wv[j][i], raw_val(rows[k + i].u, j, x), acc[j]);
+                } else if (live) {
+#pragma unroll
+                    for (int j = 0; j < V; ++j) acc[j] = fmaf(wv[j][i], past(p, j), acc[j]);
+                }
+            }
+            silu_norm<V>(acc, ng, eps);  // every lane takes part in the shuffles
+            if (live) {
+                storeVf<V>(y + t * C + c, acc);
+                if (st_out && t == t1 - 1) {  // the H newest inputs become the state
+                    float* so = st_out + ((size_t)n * C + c) * H;
+#pragma unroll
+                    for (int i = 0; i < H; ++i) {
+                        const long long p = t - (H - 1) + i;
+#pragma unroll
+                        for (int j = 0; j < V; ++j)
+                            so[j * H + i] = p >= t0 ? raw_val(rows[k + 1 + i].u, j, x) : past(p, j);
+                    }
+                }
             }
         }
         if (bad && lane == 0) set_device_error(1u);  // cu_seqlens not ascending or out of range
