@@ -477,6 +477,10 @@ def run_ours(args, world, rank, local):
     o_shape = (main["tokens"], 32, 128)
     decode = None if args.skip_decode else run_decode(args, dev, peaks, world)
     epilogue = None if args.skip_epilogue else run_epilogue(args, dev, peaks, world, o_shape)
+    gated = None
+    if epilogue is not None and args.workload == "prefill":
+        sep = main["ms_per_step"] * 1e3 + epilogue["standalone"]["us_per_launch"]
+        gated = run_gated_prefill(args, dev, peaks, world, sep)
     w = gdn_inputs.make_workload("prefill", seed=args.seed + rank)
     dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
     prologue = None if args.skip_epilogue else run_prologue(args, dev, peaks, world, w)
@@ -492,7 +496,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches, "clocks": main["clocks"], "timing": main["timing"],
         "cold_first_call": main["cold_first_call"],
         "long": legs.get("long"), "varlen": legs.get("varlen"),
-        "decode": decode, "epilogue": epilogue, "prologue": prologue, "backward": backward, "kda": kda,
+        "decode": decode, "epilogue": epilogue, "gated_prefill": gated, "prologue": prologue,
+        "backward": backward, "kda": kda,
     }
 
 
@@ -500,6 +505,48 @@ def _timing(per, mean_ms, unit_scale=1.0, unit="ms per launch"):
     t = median_ci95([x * unit_scale for x in per])
     t.update(unit=unit, mean=mean_ms * unit_scale)
     return t
+
+
+def run_gated_prefill(args, dev, peaks, world, separate_us):
+    """The prefill and the layer's output epilogue through one call
+    (gdn_chunk_fwd_gated: the prefill kernel, then the epilogue kernel in place
+    on o) on the prefill workload; `separate_us` is the sum of the two lines
+    measured on their own."""
+    import gated_deltanet_recurrence_05_b300 as gdn
+    w = gdn_inputs.make_workload("prefill", seed=args.seed)
+    lengths = w["lengths"]
+    N, T = len(lengths), sum(lengths)
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in w.items()}
+    gen = torch.Generator().manual_seed(args.seed + 99)
+    z = torch.randn(T, w["h_v"], w["d_v"], generator=gen).to(torch.bfloat16).to(dev)
+    wn = (torch.randn(w["d_v"], generator=gen) * 0.2).to(dev)
+    o = torch.empty(T, w["h_v"], w["d_v"], dtype=torch.bfloat16, device=dev)
+    fs = torch.empty(N, w["h_v"], w["d_k"], w["d_v"], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(_i=0):
+        gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], None, num_seqs=N, out=o,
+                      final_state_out=fs, gate=z, norm_weight=wn, stream=stream)
+
+    cold = cold_call(step, stream, dev)
+    for _ in range(args.warmup):
+        step()
+    ms, per = timed_launches(step, args.steps, stream, dev, world)
+    if gdn.get_device_error() != 0:
+        raise RuntimeError("device error in the gated prefill")
+    us = max_over_ranks(ms * 1e3, world, dev)
+    bytes_, flops = prefill_algorithmic(w)
+    bytes_ += z.numel() * 2 + wn.numel() * 4
+    gbs = bytes_ / (us / 1e6) / 1e9
+    tfs = flops / (us / 1e6) / 1e12
+    return {"workload": "prefill workload, then the output epilogue in place on o (bf16 gate [T, H_v, d_v], fp32 "
+                        "norm weight), one gdn_chunk_fwd_gated call per step",
+            "us_per_step": us, "tokens_per_s": T * world / (us / 1e6), "gpu_launches": 2 * args.steps,
+            "separate_us": separate_us, "timing": _timing(per, ms, 1e3, "us per step"), "cold_first_call": cold,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(bytes_),
+                         "tensor": {"achieved_tflops": round(tfs, 1), "peak_tflops": peaks["bf16_tflops"],
+                                    "frac": round(tfs / peaks["bf16_tflops"], 4)}}}
 
 
 def run_decode(args, dev, peaks, world):

@@ -57,6 +57,9 @@ def lib():
         L.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32,
                                     I32, I32, F, I32, I32, P]
         L.gdn_chunk_fwd.restype = ctypes.c_int
+        L.gdn_chunk_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, P, P, P, F, P, I32, I64, I32, I32, I32, I32,
+                                          I32, I32, F, I32, I32, P]
+        L.gdn_chunk_fwd_gated.restype = ctypes.c_int
         L.gdn_decode_step.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, I32, I32, I32, F, P]
         L.gdn_decode_step.restype = ctypes.c_int
         L.gdn_decode_step_gated.argtypes = [P, P, P, P, P, P, P, P, P, F, I32, I32, I32, I32, I32, I32,
@@ -154,13 +157,18 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
               seq_order: Optional[torch.Tensor] = None, output_dtype: Optional[torch.dtype] = None,
               scale: float = 0.0, chunk_size: int = 0, output_final_state: bool = True,
               out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None,
-              force_simt: bool = False, test_wait_timeout: bool = False, stream=None):
+              force_simt: bool = False, test_wait_timeout: bool = False,
+              gate: Optional[torch.Tensor] = None, norm_weight: Optional[torch.Tensor] = None,
+              eps: float = 1e-6, stream=None):
     """Prefill of the recurrence over packed tokens (see include/gdn.h).
 
     q, k: [T, H_qk, d_k]; v: [T, H_v, d_v] (fp32 or bf16, one dtype); g, beta:
     [T, H_v] fp32; initial_state: [N, H_v, d_k, d_v] fp32 or None; cu_seqlens:
     [N+1] int32 CUDA tensor or None (then ``num_seqs`` equal-length sequences,
-    default 1). Returns (o [T, H_v, d_v], final_state or None).
+    default 1). Returns (o [T, H_v, d_v], final_state or None). With ``gate``
+    ([T, H_v, d_v], the dtype of q/k/v) the output goes through the layer's
+    epilogue (gdn_chunk_fwd_gated: zero-centred RMSNorm with ``norm_weight``
+    [d_v] fp32 or None, times sigmoid(gate)).
     """
     N = cu_seqlens.numel() - 1 if cu_seqlens is not None else (1 if num_seqs is None else int(num_seqs))
     T, h_qk, h_v, d_k, d_v = _shapes_prefill(q, k, v, g, beta, N, initial_state)
@@ -185,12 +193,30 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
     if output_final_state:
         fs = final_state_out if final_state_out is not None else torch.empty(
             (N, h_v, d_k, d_v), dtype=torch.float32, device=v.device)
-    st = lib().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
-                             _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(fs), N, T, h_qk, h_v,
-                             d_k, d_v, _code(q), _code(o), float(scale), int(chunk_size),
-                             (FLAG_FORCE_SIMT if force_simt else 0) |
-                             (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0), _stream(stream))
-    _check("gdn_chunk_fwd", st)
+    flags = (FLAG_FORCE_SIMT if force_simt else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0)
+    if gate is None:
+        if norm_weight is not None:
+            raise ValueError("norm_weight needs a gate")
+        st = lib().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                 _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(fs), N, T, h_qk, h_v,
+                                 d_k, d_v, _code(q), _code(o), float(scale), int(chunk_size), flags,
+                                 _stream(stream))
+        _check("gdn_chunk_fwd", st)
+        return o, fs
+    _shape(gate, (T, h_v, d_v), "gate")
+    _shape(norm_weight, (d_v,), "norm_weight")
+    _dev(gate, "gate")
+    if gate.dtype != q.dtype:
+        raise TypeError("gate must have the dtype of q, k, v")
+    if norm_weight is not None:
+        _dev(norm_weight, "norm_weight")
+        if norm_weight.dtype != torch.float32:
+            raise TypeError("norm_weight must be float32")
+    st = lib().gdn_chunk_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                                   _ptr(cu_seqlens), _ptr(seq_order), _ptr(o), _ptr(gate), _ptr(norm_weight),
+                                   float(eps), _ptr(fs), N, T, h_qk, h_v, d_k, d_v, _code(q), _code(o),
+                                   float(scale), int(chunk_size), flags, _stream(stream))
+    _check("gdn_chunk_fwd_gated", st)
     return o, fs
 
 

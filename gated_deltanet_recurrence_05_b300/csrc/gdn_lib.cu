@@ -510,23 +510,31 @@ gdn_status gdn_short_conv_step(const void* x, const float* w, float* conv_state,
     return dispatch_conv_step<float>(kernel_size, x, w, conv_state, y, num_seqs, channels, norm_group, eps, s);
 }
 
-gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
-                         const float* beta, const float* initial_state, const int32_t* cu_seqlens,
-                         const int32_t* seq_order, void* o, float* final_state, int32_t num_seqs,
-                         int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
-                         int32_t dtype_qkv, int32_t dtype_o, float scale, int32_t chunk_size,
-                         int32_t flags, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// gdn_chunk_fwd with an optional output epilogue (gate != nullptr), run as a
+// second launch on o in place.
+gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                          const float* initial_state, const int32_t* cu_seqlens, const int32_t* seq_order, void* o,
+                          float* final_state, int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v,
+                          int32_t d_k, int32_t d_v, int32_t dtype_qkv, int32_t dtype_o, float scale,
+                          int32_t chunk_size, int32_t flags, const void* gate, const float* norm_weight, float eps,
+                          void* stream) {
     if (num_seqs < 0 || total_tokens < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || d_k <= 0 || d_v <= 0)
         return GDN_ERR_INVALID_ARG;
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
     if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDN_ERR_INVALID_ARG;
     if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT)) return GDN_ERR_INVALID_ARG;
+    if (gate && (!(eps >= 0.f) || !isfinite(eps))) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
     if (cu_seqlens == nullptr && total_tokens % num_seqs != 0) return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(g, 4) ||
                              !ok_ptr(beta, 4) || !ok_ptr(o, esize(dtype_o))))
         return GDN_ERR_INVALID_ARG;
+    if (gate && total_tokens > 0 && (!ok_ptr(gate, 16) || !ok_opt(norm_weight, 16))) return GDN_ERR_INVALID_ARG;
     if (!ok_opt(initial_state) || !ok_opt(final_state) || !ok_opt(cu_seqlens, 4) || !ok_opt(seq_order, 4))
         return GDN_ERR_INVALID_ARG;
     if (total_tokens > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;  // cu_seqlens are int32
@@ -547,7 +555,13 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
         const bool stall = (flags & GDN_FLAG_TEST_WAIT_TIMEOUT) != 0;
         a.max_polls = stall ? (1u << 12) : (1u << 17);
         a.withhold_chunk = stall ? 1 : -1;
-        return gdn::launch_tc(a, bf_out, s);
+        const gdn_status st = gdn::launch_tc(a, bf_out, s);
+        if (st != GDN_OK || gate == nullptr) return st;
+        // the epilogue as a second launch on o, in place (a fused output stage
+        // measured slower: it lengthens the per-chunk chain of the state warps)
+        const long long rows = total_tokens * h_v;
+        if (bf_out) return launch_gated_rmsnorm<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(o, gate, norm_weight, o, rows, d_v, eps, s);
+        return launch_gated_rmsnorm<float, __nv_bfloat16, float>(o, gate, norm_weight, o, rows, d_v, eps, s);
     }
 
     gdn::SimtArgs a{};
@@ -560,10 +574,45 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const floa
     const DevInfo di = dev_info();
     if (di.smem_optin <= 0) return GDN_ERR_CUDA;
     if (smem > (size_t)di.smem_optin) return GDN_ERR_UNSUPPORTED;
-    if (bf_in && bf_out) return launch_simt<__nv_bfloat16, __nv_bfloat16>(a, smem, s);
-    if (bf_in) return launch_simt<__nv_bfloat16, float>(a, smem, s);
-    if (bf_out) return launch_simt<float, __nv_bfloat16>(a, smem, s);
-    return launch_simt<float, float>(a, smem, s);
+    gdn_status st;
+    if (bf_in && bf_out) st = launch_simt<__nv_bfloat16, __nv_bfloat16>(a, smem, s);
+    else if (bf_in) st = launch_simt<__nv_bfloat16, float>(a, smem, s);
+    else if (bf_out) st = launch_simt<float, __nv_bfloat16>(a, smem, s);
+    else st = launch_simt<float, float>(a, smem, s);
+    if (st != GDN_OK || gate == nullptr || total_tokens == 0) return st;
+    // the epilogue as a second launch on o, in place (the gate has the dtype of q/k/v)
+    const long long rows = total_tokens * h_v;
+    if (bf_in && bf_out) return launch_gated_rmsnorm<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(o, gate, norm_weight, o, rows, d_v, eps, s);
+    if (bf_in) return launch_gated_rmsnorm<float, __nv_bfloat16, float>(o, gate, norm_weight, o, rows, d_v, eps, s);
+    if (bf_out) return launch_gated_rmsnorm<__nv_bfloat16, float, __nv_bfloat16>(o, gate, norm_weight, o, rows, d_v, eps, s);
+    return launch_gated_rmsnorm<float, float, float>(o, gate, norm_weight, o, rows, d_v, eps, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                         const int32_t* seq_order, void* o, float* final_state, int32_t num_seqs,
+                         int64_t total_tokens, int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                         int32_t dtype_qkv, int32_t dtype_o, float scale, int32_t chunk_size,
+                         int32_t flags, void* stream) {
+    return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, o, final_state, num_seqs,
+                          total_tokens, h_qk, h_v, d_k, d_v, dtype_qkv, dtype_o, scale, chunk_size, flags, nullptr,
+                          nullptr, 0.f, stream);
+}
+
+gdn_status gdn_chunk_fwd_gated(const void* q, const void* k, const void* v, const float* g,
+                               const float* beta, const float* initial_state, const int32_t* cu_seqlens,
+                               const int32_t* seq_order, void* o, const void* gate, const float* norm_weight,
+                               float eps, float* final_state, int32_t num_seqs, int64_t total_tokens,
+                               int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v, int32_t dtype_qkv,
+                               int32_t dtype_o, float scale, int32_t chunk_size, int32_t flags, void* stream) {
+    if (gate == nullptr) return GDN_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, v, g, beta, initial_state, cu_seqlens, seq_order, o, final_state, num_seqs,
+                          total_tokens, h_qk, h_v, d_k, d_v, dtype_qkv, dtype_o, scale, chunk_size, flags, gate,
+                          norm_weight, eps, stream);
 }
 
 size_t gdn_chunk_fwd_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t h_qk, int32_t h_v,

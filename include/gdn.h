@@ -132,6 +132,40 @@ gdn_status gdn_chunk_fwd(const void* q, const void* k, const void* v,
                          void* stream);
 
 /*
+ * gdn_chunk_fwd_gated -- gdn_chunk_fwd whose output goes through the output
+ * epilogue of a GDN layer (as gdn_gated_rmsnorm computes it) before it is
+ * stored: per token and value head, over the d_v features,
+ *
+ *     o = rmsnorm(S_t^T q_t scale) * (1 + norm_weight) * sigmoid(gate)
+ *
+ * (the gated delta rule followed by the zero-centred RMSNorm and the sigmoid
+ * output gate that the podcast episode "Qwen3.8-Next design: hybrid
+ * attention, residuals and n-gram embeddings", transcript segment 14, names
+ * together as the GDN layer's parts).
+ *
+ * gate        [T_total, H_v, d_v] dtype_qkv, 16-byte aligned (the caller's
+ *             x W_g; never NULL here)
+ * norm_weight [d_v] fp32, 16-byte aligned; NULL = 0 (scale 1)
+ * eps         >= 0 and finite (1e-6 is the usual value)
+ * Every other argument, and the final state, as for gdn_chunk_fwd. The
+ * epilogue runs as a second launch on o, in place, after the prefill kernel
+ * (the HBM-bound kernel of gdn_gated_rmsnorm: one more read and write of o
+ * and one read of the gate). Errors as for gdn_chunk_fwd, plus
+ * GDN_ERR_INVALID_ARG for a NULL or misaligned gate or a bad eps.
+ */
+gdn_status gdn_chunk_fwd_gated(const void* q, const void* k, const void* v,
+                               const float* g, const float* beta,
+                               const float* initial_state, const int32_t* cu_seqlens,
+                               const int32_t* seq_order,
+                               void* o, const void* gate, const float* norm_weight, float eps,
+                               float* final_state,
+                               int32_t num_seqs, int64_t total_tokens,
+                               int32_t h_qk, int32_t h_v, int32_t d_k, int32_t d_v,
+                               int32_t dtype_qkv, int32_t dtype_o,
+                               float scale, int32_t chunk_size, int32_t flags,
+                               void* stream);
+
+/*
  * gdn_chunk_fwd_workspace_size -- bytes of device scratch that gdn_chunk_fwd
  * needs for these sizes (host only, launches nothing). It is 0 for every
  * problem: both prefill kernels keep all per-chunk intermediates (the

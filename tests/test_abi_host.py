@@ -36,7 +36,7 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for need in ("gdn_chunk_fwd", "gdn_decode_step", "gdn_decode_step_gated", "gdn_gated_rmsnorm",
                  "gdn_short_conv", "gdn_short_conv_step", "gdn_chunk_bwd", "gdn_chunk_bwd_workspace_size",
-                 "gdn_chunk_fwd_workspace_size",
+                 "gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd_gated",
                  "gdn_chunk_bwd_static", "gdn_kda_chunk_fwd", "gdn_kda_decode_step",
                  "gdn_plan_seq_order",
                  "gdn_get_device_error", "gdn_status_string", "gdn_version"):
@@ -272,6 +272,19 @@ def test_chunk_bwd_workspace_size(L):
     assert f(0, 0, 1, 1, 128, 128) == 1 * st
     assert f(-1, 0, 1, 1, 128, 128) == 0 and f(1, 10, 3, 4, 128, 128) == 0
     assert gdn.chunk_bwd_workspace_size(4, 16384, 16, 32) == f(4, 16384, 16, 32, 128, 128)
+
+
+@pytest.mark.parametrize("gate,nw,eps,status", [
+    (None, None, 1e-6, INVALID),                 # the gated call needs a gate
+    (FAKE + 8, None, 1e-6, INVALID),             # gate read 16 bytes at a time
+    (FAKE, FAKE + 4, 1e-6, INVALID),             # norm weight too
+    (FAKE, None, -1.0, INVALID),                 # eps >= 0
+    (FAKE, None, float("nan"), INVALID),
+])
+def test_chunk_fwd_gated_host_validation(L, gate, nw, eps, status):
+    st = L.gdn_chunk_fwd_gated(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, gate, nw, eps, None, 1, 64, 2, 4,
+                               128, 128, 1, 1, 0.0, 0, 0, None)
+    assert st == status
 
 
 def test_chunk_fwd_workspace_size_is_zero(L):
