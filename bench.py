@@ -262,6 +262,20 @@ def timed_launches(fn, reps, stream, dev, world):
     return evs[0].elapsed_time(evs[reps]) / reps, per
 
 
+def warm_up(fn, n, stream, dev, min_seconds=0.05):
+    """At least n untimed calls, and more until `min_seconds` of them have run
+    (so that clocks have settled after any idle time). Returns the count."""
+    t = time.perf_counter()
+    k = 0
+    while k < n or time.perf_counter() - t < min_seconds:
+        fn()
+        k += 1
+        if k % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    return k
+
+
 def cold_call(fn, stream, dev):
     """Time one call that nothing has warmed (first call of this workload in
     the process): device time between events and host wall time to its end."""
@@ -401,12 +415,12 @@ def run_prefill_leg(args, name, dev, peaks, world, rank, steps, cpu_seconds, mai
         call(dd, o, fs, stream)
 
     cold = cold_call(step, stream, dev)
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    if gdn.get_device_error() != 0:
-        raise RuntimeError(f"device error during the {name} warm-up")
     with ClockSampler(dev.index) as clk:
+        # warm-up inside the sampled window, right before the timed launches
+        # (the sampler's start-up would otherwise leave the GPU idle in between)
+        warm = warm_up(step, args.warmup, stream, dev)
+        if gdn.get_device_error() != 0:
+            raise RuntimeError(f"device error during the {name} warm-up")
         ms, per = timed_launches(step, steps, stream, dev, world)
     if gdn.get_device_error() != 0:
         raise RuntimeError(f"device error during the timed {name} region")
@@ -459,6 +473,7 @@ def run_prefill_leg(args, name, dev, peaks, world, rank, steps, cpu_seconds, mai
         "value": value, "unit": "tokens/s", "ms_per_step": ms_max, "steps": steps, "config": cfg,
         "workload": cfg["workload"], "tokens": T,
         "timing": dict(median_ci95(per), unit="ms per launch", mean=ms), "cold_first_call": cold,
+        "warmup_calls_run": warm,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
         "clocks": clk.summary(),
     }
@@ -565,11 +580,9 @@ def run_decode(args, dev, peaks, world):
                         out=o, stream=stream)
 
     cold = cold_call(lambda: one(0), stream, dev)
-    for t in range(1, min(4, steps)):
-        one(t)
-    torch.cuda.synchronize(dev)
-    state.copy_(dd["state"])
     with ClockSampler(dev.index) as clk:
+        warm_up(lambda: one(1), 3, stream, dev)
+        state.copy_(dd["state"])
         ms, per = timed_launches(one, steps, stream, dev, world)
     if gdn.get_device_error() != 0:
         raise RuntimeError("device error in decode")
