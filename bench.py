@@ -472,7 +472,7 @@ def run_prefill_leg(args, name, dev, peaks, world, rank, steps, cpu_seconds, mai
     return {
         "value": value, "unit": "tokens/s", "ms_per_step": ms_max, "steps": steps, "config": cfg,
         "workload": cfg["workload"], "tokens": T,
-        "timing": dict(median_ci95(per), unit="ms per launch", mean=ms), "cold_first_call": cold,
+        "timing": _timing(per, ms), "cold_first_call": cold,
         "warmup_calls_run": warm,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": steps,
         "clocks": clk.summary(),
@@ -519,6 +519,8 @@ def run_ours(args, world, rank, local):
 def _timing(per, mean_ms, unit_scale=1.0, unit="ms per launch"):
     t = median_ci95([x * unit_scale for x in per])
     t.update(unit=unit, mean=mean_ms * unit_scale)
+    if len(per) <= 32:
+        t["samples"] = [round(x * unit_scale, 4) for x in per]
     return t
 
 

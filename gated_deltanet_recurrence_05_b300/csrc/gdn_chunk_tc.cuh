@@ -73,6 +73,7 @@ struct TcArgs {
     float scale;
     uint32_t max_polls;    // poll limit of every mbarrier wait
     int withhold_chunk;    // test of the failure path: the g/beta arrival of this chunk is never made (-1: none)
+    int nseg;              // segments per sequence (one CTA each; 1 = the whole sequence in one CTA)
 };
 
 namespace tck {
@@ -339,6 +340,53 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
     }
 }
 
+// First token that a CTA must process for a segment whose outputs start at
+// token a of a sequence that starts at s0 (one warp; every lane returns it).
+// Each token t maps a difference of two states D to alpha_t (I - beta_t k_t
+// k_t^T) D, whose spectral norm is at most c_t = alpha_t max(1, |1 - beta_t
+// |k_t|^2|) times that of D. Starting from a zero state at token ts changes
+// the state at token a - 1 by at most prod_{t=ts}^{a-1} c_t times the true
+// state before ts. The result is the nearest ts with that product below
+// 2^-40 (far below fp32 rounding), or s0 (exact: the sequence's own start)
+// when the decay never gets there, e.g. for alpha = 1.
+__device__ __forceinline__ long long segment_prefix_start(const TcArgs& p, long long s0, long long a, int h,
+                                                          int hk, int lane) {
+    constexpr float LN_EPS = -27.7258872f;  // 40 ln 2
+    const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(p.k);
+    float acc = 0.f;  // log of the product over the tokens scanned so far
+    for (long long p0 = a; p0 > s0; p0 -= 32) {
+        const long long tok = p0 - 1 - lane;  // lane 0: the token nearest to a
+        const bool valid = tok >= s0;
+        float c = 0.f;
+        if (valid) {
+            const uint4* kp = reinterpret_cast<const uint4*>(kb + ((size_t)tok * p.h_qk + hk) * D);
+            float ss = 0.f;
+#pragma unroll 4
+            for (int i = 0; i < D / 8; ++i) {
+                const uint4 u = kp[i];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                }
+            }
+            const float f = fabsf(1.f - p.beta[(size_t)tok * p.h_v + h] * ss);
+            c = p.g[(size_t)tok * p.h_v + h] + (f > 1.f ? logf(f) : 0.f);
+        }
+        float incl = c;  // sum over tokens p0 - 1 .. tok
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, valid && acc + incl <= LN_EPS);
+        if (hit) return p0 - 1 - (__ffs(hit) - 1);
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return s0;
+}
+
 template <typename TOut>
 __global__ void __launch_bounds__(NTHREADS, 1)
 chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
@@ -352,17 +400,27 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 4);
 
-    // ---- unit of work: (sequence, value head)
-    const int h = blockIdx.x % p.h_v;
-    const int pos = blockIdx.x / p.h_v;
+    // ---- unit of work: (sequence, value head, segment of the sequence). A
+    //      segment stores the outputs of tokens [seg_a, t1); it starts from a zero
+    //      state a few tokens earlier (segment_prefix_start), or from the
+    //      sequence's initial state at its first token
+    const int seg = blockIdx.x % p.nseg;
+    const int h = (blockIdx.x / p.nseg) % p.h_v;
+    const int pos = blockIdx.x / p.nseg / p.h_v;
     int n_seq;
     if (!seq_of(p.order, pos, p.num_seqs, n_seq)) return;
-    long long t0, t1;
-    if (!seq_bounds(p.cu, n_seq, p.num_seqs, p.total, p.eq_len, t0, t1)) return;
-    const int len = (int)(t1 - t0);
-    const int nc = (len + C - 1) / C;
+    long long s0, s1;  // the sequence's tokens
+    if (!seq_bounds(p.cu, n_seq, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+    const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + C - 1) / C * C;
+    const long long seg_a = s0 + seg * seg_len;
+    if (seg > 0 && seg_a >= s1) return;  // an empty segment
+    const long long t1 = seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1;
     const int hk = h / p.grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == 3) {
+        const long long ts = seg > 0 ? segment_prefix_start(p, s0, seg_a, h, hk, lane) : s0;
+        if (lane == 0) *reinterpret_cast<long long*>(sm + OFF_MISC + 8) = ts;
+    }
 #ifdef GDN_TRACE
     unsigned long long* const tb_ = blockIdx.x == 0 ? g_trace : nullptr;  // traced block
 #else
@@ -406,6 +464,11 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const long long t0 = *reinterpret_cast<const long long*>(sm + OFF_MISC + 8);  // first token processed
+    const int len = (int)(t1 - t0);
+    const int nc = (len + C - 1) / C;
+    const bool from_start = t0 == s0;  // the initial state applies
+    const bool last_seg = t1 == s1;    // this CTA ends the sequence: it writes the final state
     if (lane == 0) GDN_TRACE_AT(60, warp);
 
     auto kq_tile = [&](int n) { return sm + OFF_KQ + (uint32_t)(n % KQ_STAGES) * KQ_BYTES; };
@@ -712,7 +775,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const size_t sbase = ((size_t)n_seq * p.h_v + h) * (size_t)(D * D);
         float S[64];
-        if (p.h0) {
+        if (p.h0 && from_start) {
             const float* hp = p.h0 + sbase + (size_t)(64 * hf) * D + j;
 #pragma unroll
             for (int c = 0; c < 64; ++c) S[c] = hp[c * D];
@@ -865,6 +928,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     // o[t0 + n C + r][h][j] for r < nv: one row per register, through a
                     // byte pointer stepped by the token stride
                     const int nv = min(C, len - n * C) - 32 * hf;  // valid rows of this half
+                    // rows before token seg_a belong to the segment's prefix: not stored
+                    const long long r0 = t0 + (long long)n * C + 32 * hf;
+                    const int nskip = seg_a > r0 ? (int)min(32LL, seg_a - r0) : 0;
                     char* orow = reinterpret_cast<char*>(o + ((size_t)(t0 + (long long)n * C + 32 * hf) * p.h_v + h) * D + j);
                     const size_t ostep = (size_t)p.h_v * D * sizeof(TOut);
                     uint32_t ov[32];
@@ -875,7 +941,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     if (lane == 0) mbar_arrive(&bars[B_OFREE]);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        if (c < nv) *reinterpret_cast<TOut*>(orow) = from_f32<TOut>(__uint_as_float(ov[c]));
+                        if (c < nv && c >= nskip) *reinterpret_cast<TOut*>(orow) = from_f32<TOut>(__uint_as_float(ov[c]));
                         orow += ostep;
                     }
                 }
@@ -892,7 +958,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 64; ++c) finite = finite && (fabsf(S[c]) < INFINITY);
             if (__any_sync(0xffffffffu, !finite) && lane == 0) set_device_error(4u);
-            if (p.hT) {
+            if (p.hT && last_seg) {
                 float* hp = p.hT + sbase + (size_t)(64 * hf) * D + j;
 #pragma unroll
                 for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
@@ -956,7 +1022,7 @@ inline gdn_status launch_tc(const TcArgs& a, bool out_bf16, cudaStream_t s) {
     if (!make_head_map(&mq, a.q, a.total, a.h_qk) || !make_head_map(&mk, a.k, a.total, a.h_qk) ||
         !make_head_map(&mv, a.v, a.total, a.h_v))
         return GDN_ERR_CUDA;
-    const long long blocks = (long long)a.num_seqs * a.h_v;
+    const long long blocks = (long long)a.num_seqs * a.h_v * a.nseg;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     if (out_bf16) {
         auto kern = tck::chunk_tc_kernel<__nv_bfloat16>;

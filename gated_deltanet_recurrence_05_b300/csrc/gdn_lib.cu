@@ -526,7 +526,7 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         return GDN_ERR_INVALID_ARG;
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
     if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDN_ERR_INVALID_ARG;
-    if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT)) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT | GDN_FLAG_NO_SPLIT)) return GDN_ERR_INVALID_ARG;
     if (gate && (!(eps >= 0.f) || !isfinite(eps))) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
@@ -555,6 +555,20 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         const bool stall = (flags & GDN_FLAG_TEST_WAIT_TIMEOUT) != 0;
         a.max_polls = stall ? (1u << 12) : (1u << 17);
         a.withhold_chunk = stall ? 1 : -1;
+        // Fewer (sequence, head) units than SMs: split each sequence into
+        // segments of at least 512 tokens, one CTA each (the kernel starts a
+        // segment from a zero state where the decay has made the earlier
+        // tokens' influence negligible, else from the sequence start). Not
+        // when the final state overwrites the initial state: a later segment
+        // could then finish before an earlier one has read it.
+        a.nseg = 1;
+        if (!(flags & GDN_FLAG_NO_SPLIT) && !(final_state != nullptr && final_state == initial_state)) {
+            const long long units = (long long)num_seqs * h_v, sms = std::max(dev_info().sms, 1);
+            if (units < sms) {
+                const long long by_len = (long long)(total_tokens / num_seqs) / 512;
+                a.nseg = (int)std::max(1LL, std::min(std::min(sms / units, by_len), 64LL));
+            }
+        }
         const gdn_status st = gdn::launch_tc(a, bf_out, s);
         if (st != GDN_OK || gate == nullptr) return st;
         // the epilogue as a second launch on o, in place (a fused output stage

@@ -235,7 +235,8 @@ def test_full_varlen_workload_all_pairs():
 
 @pytest.mark.slow
 def test_full_long_prefill_all_pairs():
-    """B=1, T=65536, initial state N(0, 0.02): all 32 pairs."""
+    """B=1, T=65536, initial state N(0, 0.02): all 32 pairs (32 units for 148
+    SMs: the tensor-core path splits the sequence into segments)."""
     _full_size_all_pairs(gdn_inputs.make_workload("long"), "long")
 
 
@@ -278,3 +279,45 @@ def test_large_values_inside_fp16_range_stay_within_tolerance():
     o_ref, S_ref = _ref(d)
     assert_parity(o, o_ref, TAU_BF16, "o")
     assert_parity(S, S_ref, TAU_BF16, "final state")
+
+
+def _run_split(d, split):
+    dd = to_cuda(d)
+    o, S = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], dd["cu_seqlens"],
+                         output_dtype=torch.float32, split=split)
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    return o.cpu().numpy(), S.cpu().numpy()
+
+
+def test_sequence_segments_without_decay_are_bit_exact():
+    """alpha = 1 (g = 0): no prefix ever reaches the 2^-40 bound, so every
+    segment restarts at its sequence's first token with the initial state and
+    computes exactly what the unsplit kernel computes for its tokens."""
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16",
+                                lengths=[3000, 2100], h0_std=0.02, seed=61)
+    d["g"].zero_()
+    o1, S1 = _run_split(d, True)
+    o2, S2 = _run_split(d, False)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+@pytest.mark.parametrize("k_scale", [1.0, 1.5])
+def test_sequence_segments_match_oracle(k_scale):
+    """Fewer (sequence, head) units than SMs: the sequences are split into
+    segments, each started from a zero state where the decay bound allows
+    (unit keys: beta |k|^2 < 1; keys of norm 1.5: factors |1 - beta |k|^2| up
+    to 1.25 lengthen the prefixes). Every output and final state against the
+    oracle and against the unsplit kernel."""
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16",
+                                lengths=[3000, 1, 0, 1500, 700, 2600], h0_std=0.02, seed=62)
+    if k_scale != 1.0:
+        d["k"] = (d["k"].float() * k_scale).to(torch.bfloat16)
+    o, S = _run_split(d, True)
+    o_ref, S_ref = _ref(d)
+    assert_parity(o, o_ref, TAU_BF16, "o")
+    assert_parity(S, S_ref, TAU_BF16, "final state")
+    o2, S2 = _run_split(d, False)
+    assert_parity(o, o2, TAU_BF16, "o vs unsplit")
+    assert_parity(S, S2, TAU_BF16, "final state vs unsplit")

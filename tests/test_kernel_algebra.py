@@ -10,7 +10,12 @@ out here from its statement in the kernel's header comment).
   - decode kernel (gdn_decode.cuh): one pass over S gives S^T k and S^T q, and
     o = scale (alpha S^T q + (k . q) u);
   - KDA kernels (gdn_kda.cuh): the reads use a o k and a o q against the
-    undecayed state and o = scale (S^T (a o q) + (k . q) u).
+    undecayed state and o = scale (S^T (a o q) + (k . q) u);
+  - sequence segments of the tensor-core prefill (gdn_chunk_tc.cuh,
+    segment_prefix_start): a segment that starts from a zero state at the
+    nearest token ts where prod_{t=ts}^{a-1} alpha_t max(1, |1 - beta_t
+    |k_t|^2|) <= 2^-40 reaches its first token a with a state within 2^-40
+    times the spectral norm of the true state before ts.
 """
 import math
 
@@ -133,3 +138,57 @@ def test_kda_single_pass_rearrangement():
                                         h0=S[None, None], scale=scale)
     np.testing.assert_allclose(o, o_ref[0, 0], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(S_new, S_ref[0, 0], rtol=1e-12, atol=1e-14)
+
+
+def _prefix_start(g, beta, k, s0, a, ln_eps=-40 * math.log(2.0)):
+    """The segment rule, written out token by token (fp64)."""
+    acc = 0.0
+    for t in range(a - 1, s0 - 1, -1):
+        f = abs(1.0 - beta[t] * float(k[t] @ k[t]))
+        acc += g[t] + (math.log(f) if f > 1.0 else 0.0)
+        if acc <= ln_eps:
+            return t
+    return s0
+
+
+@pytest.mark.parametrize("g_shift,k_scale", [(0.0, 1.0), (2.0, 1.0), (-5.0, 1.0), (0.0, 2.0), (None, 1.0)])
+def test_segment_prefix_bound(g_shift, k_scale):
+    """Run the rule (fp64, this file's own loop) from the exact state and from
+    a zero state at the prefix start; at the segment's first token the two
+    states differ by at most 2^-40 times the spectral norm of the true state
+    before the prefix (the product of the per-token factors bounds the
+    spectral norm of the map that carries a state difference forward)."""
+    rng = np.random.default_rng(7)
+    L, dk, dv = 3000, 16, 8
+    k = rng.standard_normal((L, dk))
+    k = k / np.linalg.norm(k, axis=1, keepdims=True) * k_scale
+    v = rng.standard_normal((L, dv))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(L)))
+    if g_shift is None:
+        g = np.zeros(L)                      # alpha = 1: no bound is ever reached
+    else:
+        g = -np.log1p(np.exp(rng.standard_normal(L) + g_shift))
+    S0 = rng.standard_normal((dk, dv)) * 0.5
+    states = [S0]
+    S = S0.copy()
+    for t in range(L):
+        a_ = math.exp(g[t])
+        S = a_ * S + beta[t] * np.outer(k[t], v[t] - a_ * (S.T @ k[t]))
+        states.append(S)                     # states[t + 1] = state after token t
+    for seg_a in (700, 1500, 2999):
+        ts = _prefix_start(g, beta, k, 0, seg_a)
+        if g_shift is None:
+            assert ts == 0                   # exact: the segment starts at the sequence start
+            continue
+        # the sequence's start: its initial state (exact); elsewhere a zero state
+        Z = S0.copy() if ts == 0 else np.zeros((dk, dv))
+        for t in range(ts, seg_a):
+            a_ = math.exp(g[t])
+            Z = a_ * Z + beta[t] * np.outer(k[t], v[t] - a_ * (Z.T @ k[t]))
+        bound = 0.0 if ts == 0 else 2.0 ** -40 * np.linalg.norm(states[ts], 2)
+        err = np.linalg.norm(Z - states[seg_a], 2)
+        fp64 = 1e-12 * np.linalg.norm(states[seg_a], 2)  # rounding of the two fp64 runs
+        assert err <= bound + fp64, (g_shift, k_scale, seg_a, ts, err, bound)
+        # and the rule does not start earlier than it needs to
+        if ts > 0 and ts < seg_a - 1:
+            assert _prefix_start(g, beta, k, ts + 1, seg_a) == ts + 1  # one token fewer misses the bound
