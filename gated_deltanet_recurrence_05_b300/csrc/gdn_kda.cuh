@@ -136,7 +136,51 @@ struct Args {
     long long total, eq_len;
     int num_seqs, h_qk, h_v, grp;
     float scale;
+    int nseg;          // segments per sequence (one CTA each; 1 = the whole sequence)
 };
+
+// First token to process for a segment whose outputs start at token a of a
+// sequence starting at s0 (one warp; every lane returns it). Token t maps a
+// difference of states D to (I - beta_t k_t k_t^T) diag(alpha_t) D, whose
+// spectral norm is at most max_i alpha_ti max(1, |1 - beta_t |k_t|^2|) times
+// that of D; the result is the nearest ts at which the product of these
+// factors over ts .. a - 1 is below 2^-40, or s0 (exact) if it never is.
+template <typename TIn>
+__device__ __forceinline__ long long segment_prefix_start(const Args& p, long long s0, long long a, int h, int hk,
+                                                          int lane) {
+    constexpr float LN_EPS = -27.7258872f;  // 40 ln 2
+    const TIn* k = static_cast<const TIn*>(p.k);
+    float acc = 0.f;
+    for (long long p0 = a; p0 > s0; p0 -= 32) {
+        const long long tok = p0 - 1 - lane;
+        const bool valid = tok >= s0;
+        float c = 0.f;
+        if (valid) {
+            const float* gp = p.g + ((size_t)tok * p.h_v + h) * D;
+            const TIn* kp = k + ((size_t)tok * p.h_qk + hk) * D;
+            float gmax = -INFINITY, ss = 0.f;
+#pragma unroll 4
+            for (int i = 0; i < D; i += 4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gp + i);
+                gmax = fmaxf(gmax, fmaxf(fmaxf(g4.x, g4.y), fmaxf(g4.z, g4.w)));
+                const float4 k4 = load4(kp + i);
+                ss = fmaf(k4.x, k4.x, fmaf(k4.y, k4.y, fmaf(k4.z, k4.z, fmaf(k4.w, k4.w, ss))));
+            }
+            const float f = fabsf(1.f - p.beta[(size_t)tok * p.h_v + h] * ss);
+            c = gmax + (f > 1.f ? logf(f) : 0.f);
+        }
+        float incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, valid && acc + incl <= LN_EPS);
+        if (hit) return p0 - 1 - (__ffs(hit) - 1);
+        acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return s0;
+}
 
 template <typename TIn>
 __device__ __forceinline__ void kda_stage(float* sm, const Args& p, long long tb0, int n, int h, int hk) {
@@ -179,22 +223,40 @@ __device__ __forceinline__ void kda_stage(float* sm, const Args& p, long long tb
     if (threadIdx.x < BLK) sm[OFF_B + threadIdx.x] = threadIdx.x < n ? p.beta[(size_t)(tb0 + threadIdx.x) * p.h_v + h] : 0.f;
 }
 
+// Two CTAs fit on an SM (at most 128 registers per thread, 91 KB of shared
+// memory): when the (sequence, value head) units are fewer than twice the
+// SMs, each sequence is split into segments (one CTA each), started a few
+// tokens early from a zero state where the decay allows it
+// (segment_prefix_start), so that more warps share each SM.
 template <typename TIn, typename TOut>
-__global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Args p) {
+__global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
     extern __shared__ float4 smem_f4[];
+    __shared__ long long seg_start;
     float* sm = reinterpret_cast<float*>(smem_f4);
-    const int pos = blockIdx.x / p.h_v, h = blockIdx.x - pos * p.h_v, hk = h / p.grp;
+    const int seg = blockIdx.x % p.nseg, unit = blockIdx.x / p.nseg;
+    const int pos = unit / p.h_v, h = unit - pos * p.h_v, hk = h / p.grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = warp * 16, c0 = lane * 4;
     int n = 0;
-    long long t0 = 0, t1 = 0;
+    long long s0 = 0, s1 = 0;
     if (!seq_of(p.order, pos, p.num_seqs, n)) return;
-    if (!seq_bounds(p.cu, n, p.num_seqs, p.total, p.eq_len, t0, t1)) return;
+    if (!seq_bounds(p.cu, n, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+    // this CTA stores the outputs of tokens [seg_a, t1)
+    const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + BLK - 1) / BLK * BLK;
+    const long long seg_a = s0 + seg * seg_len;
+    if (seg > 0 && seg_a >= s1) return;  // an empty segment
+    const long long t1 = seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1;
+    if (warp == 0) {
+        const long long ts = seg > 0 ? segment_prefix_start<TIn>(p, s0, seg_a, h, hk, lane) : s0;
+        if (lane == 0) seg_start = ts;
+    }
+    __syncthreads();
+    const long long t0 = seg_start;  // first token processed
     const size_t st_off = ((size_t)n * p.h_v + h) * D * D;
     TOut* o = static_cast<TOut*>(p.o);
 
     float S[16][4];
-    if (p.h0) bwd::load_state(S, p.h0 + st_off, r0, c0);
+    if (p.h0 && t0 == s0) bwd::load_state(S, p.h0 + st_off, r0, c0);
     else bwd::zero_state(S);
     for (long long tb0 = t0; tb0 < t1; tb0 += BLK) {
         const int nt = (int)min((long long)BLK, t1 - tb0);
@@ -235,7 +297,8 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Args p) {
                 if (part == 0) {
                     const float uu = sm[OFF_B + j] * (sm[OFF_V + j * D + colx] - sk);
                     sm[OFF_U + colx] = uu;
-                    o[((size_t)(tb0 + j) * p.h_v + h) * D + colx] = from_f32<TOut>(p.scale * fmaf(sm[OFF_KQ + j], uu, sq));
+                    if (tb0 + j >= seg_a)  // the segment's prefix tokens are not stored
+                        o[((size_t)(tb0 + j) * p.h_v + h) * D + colx] = from_f32<TOut>(p.scale * fmaf(sm[OFF_KQ + j], uu, sq));
                 }
             }
             __syncthreads();
@@ -253,7 +316,7 @@ __global__ void __launch_bounds__(NT, 1) kda_prefill_kernel(const Args p) {
             }
         }
     }
-    if (p.hT) bwd::store_state(S, p.hT + st_off, r0, c0);
+    if (p.hT && t1 == s1) bwd::store_state(S, p.hT + st_off, r0, c0);  // the last segment
 }
 
 }  // namespace kda

@@ -235,14 +235,26 @@ gdn_status launch_bwd(gdn::bwd::Args a, float* dq, float* dk, char* ws, const Bw
 namespace {
 
 template <typename TIn, typename TOut>
-gdn_status launch_kda_prefill(const gdn::kda::Args& a, cudaStream_t s) {
-    const long long blocks = (long long)a.num_seqs * a.h_v;
-    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
+gdn_status launch_kda_prefill(gdn::kda::Args a, cudaStream_t s) {
     const DevInfo di = dev_info();
+    // fewer units than two per SM: sequence segments (not when the final
+    // state overwrites the initial state: a later segment could then finish
+    // before an earlier one has read it)
+    a.nseg = 1;
+    const long long units = (long long)a.num_seqs * a.h_v, slots = 2LL * std::max(di.sms, 1);
+    if (units > 0 && units < slots && !(a.hT != nullptr && a.hT == a.h0)) {
+        const long long by_len = (long long)(a.total / a.num_seqs) / 512;
+        a.nseg = (int)std::max(1LL, std::min(std::min(slots / units, by_len), 64LL));
+    }
+    const long long blocks = units * a.nseg;
+    if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     if (di.smem_optin < (int)gdn::kda::SMEM_BYTES) return di.smem_optin <= 0 ? GDN_ERR_CUDA : GDN_ERR_UNSUPPORTED;
     auto kern = gdn::kda::kda_prefill_kernel<TIn, TOut>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gdn::kda::SMEM_BYTES) !=
         cudaSuccess)
+        return GDN_ERR_CUDA;
+    // the largest shared-memory carve-out, so that two CTAs fit on an SM
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return GDN_ERR_CUDA;
     kern<<<(unsigned)blocks, gdn::kda::NT, gdn::kda::SMEM_BYTES, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

@@ -46,6 +46,21 @@ def test_prefill_bf16_varlen_gqa_edges():
     assert_parity(S, S_ref, TAU_F32, "final state")
 
 
+def test_prefill_sequence_segments():
+    """Fewer (sequence, head) units than two per SM and long sequences: the
+    prefill splits each sequence into segments, the later ones started from a
+    zero state where the slowest channel's decay has shrunk the earlier tokens'
+    influence below 2^-40 (see the header). Every output and final state
+    against the oracle, at the fp32 bound."""
+    d = gdn_inputs.make_prefill(h_qk=1, h_v=2, d_k=128, d_v=128, dtype="bf16",
+                                lengths=[3000, 1, 1500, 700], h0_std=0.02, seed=44)
+    g = gdn_inputs.make_channel_decay((sum(d["lengths"]), 2, 128), seed=44)
+    o, S = _kda_gpu(d, g)
+    o_ref, S_ref = oracle.kda_recurrent(d["q"], d["k"], d["v"], g, d["beta"], h0=d["h0"], cu_seqlens=_cu(d))
+    assert_parity(o, o_ref, TAU_F32, "o")
+    assert_parity(S, S_ref, TAU_F32, "final state")
+
+
 def test_prefill_fp32_equal_length_bf16_output_and_order():
     d = gdn_inputs.make_prefill(h_qk=2, h_v=2, d_k=128, d_v=128, dtype="f32", batch=3, seqlen=45, seed=42)
     g = gdn_inputs.make_channel_decay((135, 2, 128), g_shift=-3.0, seed=42)
