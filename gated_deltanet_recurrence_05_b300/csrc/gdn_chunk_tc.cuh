@@ -905,13 +905,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!WAITW(B_SREADY, n & 1)) break;
                 if (ws == 0 && lane == 0) GDN_TRACE_AT(11, n);
                 tc_fence_after();
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t acc[32];
-                    tmem_ld32(tmem + lane_base + T_SACC + 64 * hf + 32 * q, acc);
+                {
+                    uint32_t acc0[32], acc1[32];
+                    tmem_ld32(tmem + lane_base + T_SACC + 64 * hf, acc0);
+                    tmem_ld32(tmem + lane_base + T_SACC + 64 * hf + 32, acc1);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) S[32 * q + c] = fmaf(gC, S[32 * q + c], __uint_as_float(acc[c]));
+                    for (int c = 0; c < 32; ++c) S[c] = fmaf(gC, S[c], __uint_as_float(acc0[c]));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gC, S[32 + c], __uint_as_float(acc1[c]));
                 }
                 put_state_f16();
                 tc_fence_before();
