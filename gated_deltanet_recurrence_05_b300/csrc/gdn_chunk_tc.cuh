@@ -837,6 +837,26 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (lane == 0) mbar_arrive(&bars[B_CONV0 + (m & 1)]);
             return true;
         };
+        // -W^T of chunk m from TMEM (lane = key index i = j, columns = chunk
+        // rows r; this thread: rows 32 hf .. + 31) into the MN-major fp16 B
+        // tile of M3a, once M2w(m) has run; M3a(m - 1) has finished reading
+        // the tile (DREADY(m - 1) was seen before every call)
+        auto handoff_w = [&](int m) -> bool {
+            if (!WAITW(B_M2W0 + (m & 1), (m >> 1) & 1)) return false;
+            tc_fence_after();
+            {
+                uint32_t w[32];
+                tmem_ld32(tmem + lane_base + T_W + 32 * hf, w);
+                tmem_ld_wait();
+                store_half_row_sw128(sm + OFF_WT, (uint32_t)j, reinterpret_cast<const float*>(w), hf);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_WREADY]);
+            if (ws == 0 && lane == 0) GDN_TRACE_AT(13, m);
+            return true;
+        };
         TOut* o = static_cast<TOut*>(p.o);
         // conversions run two chunks ahead of the state: chunk n + 2 after the
         // output of chunk n (iterations n = -2, -1 only convert chunks 0, 1);
@@ -879,24 +899,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[B_DELTA]);
             }
-            // -W^T of chunk n + 1 from TMEM (lane = key index i = j, columns =
-            // chunk rows r; this thread: rows 32 hf .. + 31) into the MN-major
-            // fp16 B tile of M3a, once M2w(n + 1) has run; M3a(n) has finished
-            // reading the tile (DREADY(n) was seen). Runs while M5(n) does.
-            if (n + 1 >= 0 && n + 1 < nc) {
-                if (!WAITW(B_M2W0 + ((n + 1) & 1), ((n + 1) >> 1) & 1)) break;
-                tc_fence_after();
-                {
-                    uint32_t w[32];
-                    tmem_ld32(tmem + lane_base + T_W + 32 * hf, w);
-                    tmem_ld_wait();
-                    store_half_row_sw128(sm + OFF_WT, (uint32_t)j, reinterpret_cast<const float*>(w), hf);
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[B_WREADY]);
-                if (ws == 0 && lane == 0) GDN_TRACE_AT(13, n + 1);
+            // -W^T of chunk n + 1: handed over now, while M5(n) runs, if M2w(n + 1)
+            // has already finished; otherwise after this chunk's state update
+            // and output, so that a late prep does not hold those back
+            bool w_pending = n + 1 >= 0 && n + 1 < nc;
+            if (w_pending &&
+                (n < 0 || __all_sync(0xffffffffu, mbar_test(&bars[B_M2W0 + ((n + 1) & 1)], ((n + 1) >> 1) & 1)))) {
+                if (!handoff_w(n + 1)) break;
+                w_pending = false;
             }
             if (n >= 0) {
                 const float* gb = gb_slot(n);
@@ -948,6 +958,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                     }
                 }
             }
+            if (w_pending && !handoff_w(n + 1)) break;
             if (n + 2 < nc && !convert(n + 2)) break;
             if (n >= 0 && ws == 0 && lane == 0) GDN_TRACE_AT(14, n);
         }
