@@ -84,9 +84,10 @@ def kernel_sha():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per prefill launch from the committed ncu summary, or None if
-    the summary is absent or was taken on other kernel sources."""
+def recorded_traffic(key="dram_bytes_per_launch"):
+    """DRAM bytes per prefill launch from the committed ncu summary (`key`: the
+    prefill workload's, or `dram_bytes_per_launch_long`), or None if the
+    summary is absent or was taken on other kernel sources."""
     try:
         kv = {}
         with open(TRAFFIC_FILE) as f:
@@ -96,7 +97,7 @@ def recorded_traffic():
                     kv[k.strip()] = v.strip()
         if kv.get("kernel_sha256") != kernel_sha():
             return None
-        return float(kv["dram_bytes_per_launch"])
+        return float(kv[key])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -248,10 +249,15 @@ def timed_launches(fn, reps, stream, dev, world):
     """Run fn(i) for i < reps on `stream` with one CUDA event before each call
     and one after the last (all on the launching stream), bracketed by a
     barrier and device synchronisations. Returns (mean ms per call over the
-    whole bracketed region, list of per-call ms)."""
+    whole bracketed region, list of per-call ms). The calls must be issued on
+    the current stream (where the spin runs)."""
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
     barrier(world)
     torch.cuda.synchronize(dev)
+    # a short device-side spin before the first event, so that the host has
+    # queued the first launches by the time it ends: the events then time the
+    # device work, not the host's latency to enqueue the first call
+    torch.cuda._sleep(2_000_000)
     for i in range(reps):
         evs[i].record(stream)
         fn(i)
@@ -433,7 +439,9 @@ def run_prefill_leg(args, name, dev, peaks, world, rank, steps, cpu_seconds, mai
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(gbs / peaks["hbm_gbs"], 4),
-                "traffic": (args.traffic if args.traffic is not None else recorded_traffic()) if main else None,
+                "traffic": (args.traffic if main and args.traffic is not None else
+                            recorded_traffic() if name == "prefill" else
+                            recorded_traffic("dram_bytes_per_launch_long") if name == "long" else None),
                 "peak_source": PEAK_SOURCE, "algorithmic_bytes_per_launch": int(bytes_),
                 "arithmetic_intensity_flop_per_byte": round(flops / bytes_, 1),
                 "ridge_flop_per_byte": round(ridge, 1),
