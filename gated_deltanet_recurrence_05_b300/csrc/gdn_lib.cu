@@ -123,7 +123,11 @@ gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32
     const int cblocks = v8 ? C / 256 : (C + 127) / 128;
     if (runs > 0) {
         if (cblocks > 65535) return GDN_ERR_UNSUPPORTED;
-        auto kern = v8 ? gdn::short_conv_kernel<T, K, 8> : gdn::short_conv_kernel<T, K, 4>;
+        // the head size of q and k (128) and no norm (v) are compiled as constants
+        auto kern = v8 ? (ng == 0 ? gdn::short_conv_kernel<T, K, 8, 0>
+                                  : ng == 128 ? gdn::short_conv_kernel<T, K, 8, 128> : gdn::short_conv_kernel<T, K, 8, -1>)
+                       : (ng == 0 ? gdn::short_conv_kernel<T, K, 4, 0>
+                                  : ng == 128 ? gdn::short_conv_kernel<T, K, 4, 128> : gdn::short_conv_kernel<T, K, 4, -1>);
         int per_sm = 0;  // one resident wave over all channel blocks
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1)
             per_sm = 1;

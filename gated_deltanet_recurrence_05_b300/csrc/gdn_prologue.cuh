@@ -64,16 +64,23 @@ template <int V, typename T> __device__ __forceinline__ void storeVf(T* p, const
 }
 
 // silu, then the L2 norm over groups of `ng` channels (ng = 0: none; else a
-// power of two, at least V, dividing 32 V: the group spans ng / V lanes)
-template <int V>
+// power of two, at least V, dividing 32 V: the group spans ng / V lanes). NG
+// fixes the group at compile time: 0 (no norm), a group size, or -1 (ng).
+template <int V, int NG = -1>
 __device__ __forceinline__ void silu_norm(float* s, int ng, float eps) {
 #pragma unroll
     for (int j = 0; j < V; ++j) s[j] = silu_f(s[j]);
-    if (ng) {
+    const int g = NG >= 0 ? NG : ng;
+    if (g) {
         float ss = 0.f;
 #pragma unroll
         for (int j = 0; j < V; ++j) ss = fmaf(s[j], s[j], ss);
-        for (int off = 1; off < ng / V; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if constexpr (NG > 0) {
+#pragma unroll
+            for (int off = 1; off < NG / V; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        } else {
+            for (int off = 1; off < g / V; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        }
         const float r = rsqrtf(ss + eps);
 #pragma unroll
         for (int j = 0; j < V; ++j) s[j] *= r;
@@ -132,7 +139,7 @@ __device__ __forceinline__ float raw_val(const uint32_t* u, int j, const float*)
 // sequence's first token come from the caller's conv state (or are zero), and
 // a tile may span several sequences. The warp that holds a sequence's last
 // token writes that sequence's final conv state.
-template <typename T, int K, int V>
+template <typename T, int K, int V, int NG>
 __global__ void __launch_bounds__(256)
 short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __restrict__ y,
                   const int32_t* __restrict__ cu, const float* __restrict__ st_in, float* __restrict__ st_out,
@@ -183,7 +190,7 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
                     for (int i = 1; i < K; ++i) a = fmaf(wv[j][i], win[i][j], a);
                     acc[j] = a;
                 }
-                silu_norm<V>(acc, ng, eps);
+                silu_norm<V, NG>(acc, ng, eps);
                 if (live) storeVf<V>(yp, acc);
                 yp += C;
 #pragma unroll
@@ -230,7 +237,7 @@ short_conv_kernel(const T* __restrict__ x, const float* __restrict__ w, T* __res
                     for (int j = 0; j < V; ++j) acc[j] = fmaf(wv[j][i], past(p, j), acc[j]);
                 }
             }
-            silu_norm<V>(acc, ng, eps);  // every lane takes part in the shuffles
+            silu_norm<V, NG>(acc, ng, eps);  // every lane takes part in the shuffles
             if (live) {
                 storeVf<V>(y + t * C + c, acc);
                 if (st_out && t == t1 - 1) {  // the H newest inputs become the state
