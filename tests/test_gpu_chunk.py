@@ -321,3 +321,26 @@ def test_sequence_segments_match_oracle(k_scale):
     o2, S2 = _run_split(d, False)
     assert_parity(o, o2, TAU_BF16, "o vs unsplit")
     assert_parity(S, S2, TAU_BF16, "final state vs unsplit")
+
+
+def test_bf16_output_segments_and_unaligned_buffer():
+    """bf16 outputs with sequence segments (the rows of a segment's prefix are
+    not stored) into a 16-byte aligned and a 2-byte aligned buffer: both
+    against the oracle, and equal to each other bit for bit. Ragged lengths,
+    GQA 2:1."""
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16",
+                                lengths=[3000, 1, 0, 1500, 77, 700], h0_std=0.02, seed=63)
+    dd = to_cuda(d)
+    T = sum(d["lengths"])
+    outs = []
+    for offset in (0, 1):  # elements: 0 = 16-byte aligned, 1 = 2-byte aligned
+        buf = torch.full((T * 4 * 128 + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        out = buf[offset:offset + T * 4 * 128].view(T, 4, 128)
+        assert (out.data_ptr() % 16 == 0) == (offset == 0)
+        gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], dd["cu_seqlens"], out=out)
+        torch.cuda.synchronize()
+        assert gdn.get_device_error() == 0
+        outs.append(out.float().cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    o_ref, _ = _ref(d)
+    assert_parity(outs[0], o_ref, TAU_BF16, "o (bf16)", out_bf16=True)
