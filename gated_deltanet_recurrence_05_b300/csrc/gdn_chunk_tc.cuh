@@ -121,9 +121,10 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 enum {
     B_FULL_KQ = 0, B_EMPTY_KQ = 3, B_FULL_V = 6, B_EMPTY_V = 8, B_GB_FULL = 10, B_GB_EMPTY = 13,
     B_XREADY0 = 16, B_XREADY1, B_XFREE, B_BWU0, B_BWU1, B_M2W0, B_M2W1, B_WREADY, B_DREADY, B_DELTA,
-    B_SREADY, B_STREADY, B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE, B_CONV0, B_CONV1, B_M2U0, B_M2U1
+    B_SREADY, B_STREADY, B_OREADY, B_OFREE, B_PFREE0, B_PFREE1, B_DONE, B_CONV0, B_CONV1, B_M2U0, B_M2U1,
+    B_VCONV0, B_VCONV1
 };
-static_assert(B_M2U1 < (int)NUM_BARS, "barrier count");
+static_assert(B_VCONV1 < (int)NUM_BARS, "barrier count");
 
 // gb slot fields (float offsets)
 constexpr int GB_G = 0, GB_GAM = 64, GB_BET = 128, GB_BG = 192, GB_DEC = 256, GB_QSC = 320, GB_GC = 384;
@@ -444,6 +445,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         mbar_init(&bars[B_BWU0], 4); mbar_init(&bars[B_BWU1], 4);
         mbar_init(&bars[B_M2W0], 1); mbar_init(&bars[B_M2W1], 1); mbar_init(&bars[B_WREADY], 8);
         mbar_init(&bars[B_M2U0], 1); mbar_init(&bars[B_M2U1], 1);
+        mbar_init(&bars[B_VCONV0], 1); mbar_init(&bars[B_VCONV1], 1);
         mbar_init(&bars[B_DREADY], 1); mbar_init(&bars[B_DELTA], 8); mbar_init(&bars[B_SREADY], 1);
         mbar_init(&bars[B_STREADY], 8); mbar_init(&bars[B_OREADY], 1); mbar_init(&bars[B_OFREE], 8);
         mbar_init(&bars[B_PFREE0], 1); mbar_init(&bars[B_PFREE1], 1); mbar_init(&bars[B_DONE], 2);
@@ -541,7 +543,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 // program order after M5(n-1) (so Delta(n-1) has been read out)
                 // and before M3a(n), which accumulates onto it; needs T of chunk
                 // n (BWU) and the fp16 V (CONV).
-                if (!WAIT(B_CONV0 + (n & 1), (n >> 1) & 1) || !WAIT(B_BWU0 + (n & 1), (n >> 1) & 1)) break;
+                if (!WAIT(B_CONV0 + (n & 1), (n >> 1) & 1) || !WAIT(B_VCONV0 + (n & 1), (n >> 1) & 1) ||
+                    !WAIT(B_BWU0 + (n & 1), (n >> 1) & 1))
+                    break;
                 tc_fence_after();
                 {
                     const uint32_t vt = smem_u32(v_tile(n));
@@ -647,7 +651,31 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     } else if (warp == 3) {
         // ------------------------------------- g, beta -> decay factors per chunk
         regs_dec<REGS_ROLES>();
-        for (int n = 0; n < nc; ++n) {
+        // V of chunk m (bf16 -> fp16 in place, the B operand of M2u) once its
+        // TMA load has landed: 1024 16-byte units, 32 per lane
+        auto convert_v = [&](int m) -> bool {
+            if (!WAITW(B_FULL_V + m % V_STAGES, (m / V_STAGES) & 1)) return false;
+            uint4* base = reinterpret_cast<uint4*>(v_tile(m));
+#pragma unroll 1
+            for (int k = 0; k < 32; k += 4) {
+                uint4 u[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) u[i] = base[lane + 32 * (k + i)];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 a = unbf2(u[i].x), b2 = unbf2(u[i].y), c = unbf2(u[i].z), d = unbf2(u[i].w);
+                    base[lane + 32 * (k + i)] = make_uint4(h2(a.x, a.y), h2(b2.x, b2.y), h2(c.x, c.y), h2(d.x, d.y));
+                }
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_VCONV0 + (m & 1)]);
+            return true;
+        };
+        // chunk n's decay factors, then the V tile of chunk n - 1 (one more
+        // chunk of time for its load to land)
+        for (int n = 0; n <= nc; ++n) {
+          if (n < nc) {
             const int slot = n % GB_SLOTS;
             if (n >= GB_SLOTS && !WAITW(B_GB_EMPTY + slot, ((n / GB_SLOTS) - 1) & 1)) break;
             float* gb = gb_slot(n);
@@ -683,6 +711,8 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             // (a failure-path test withholds one arrival: every wait on it runs out)
             if (lane == 0 && n != p.withhold_chunk) mbar_arrive(&bars[B_GB_FULL + slot]);
             if (lane == 0) GDN_TRACE_AT(41, n);
+          }
+          if (n >= 1 && !convert_v(n - 1)) break;
         }
     } else if (warp < 8) {
         // ----------------------------------------------------------------- prep
@@ -798,30 +828,30 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_STREADY]);
         // bf16 -> fp16 operands of chunk m, in place (K as it is and Q times
-        // gamma scale once M1(m) has consumed the bf16 K and Q; V as it is):
-        // 3 tiles x 128 row halves of 64 values over the 256 state threads
+        // gamma scale once M1(m) has consumed the bf16 K and Q): 2 tiles x
+        // 128 row halves of 64 values over the 256 state threads
         const int ts = 32 * ws + lane;
         auto convert = [&](int m) -> bool {
             if (!WAITW(B_GB_FULL + m % GB_SLOTS, (m / GB_SLOTS) & 1) ||
-                !WAITW(B_XREADY0 + (m & 1), (m >> 1) & 1) || !WAITW(B_FULL_V + m % V_STAGES, (m / V_STAGES) & 1))
+                !WAITW(B_XREADY0 + (m & 1), (m >> 1) & 1))
                 return false;
-            // 16-byte units u = ts + 256 k, k = 0..11: the K, Q stage (K kb0 | Q kb0
+            // 16-byte units u = ts + 256 k, k = 0..7 of the K, Q stage (K kb0 | Q kb0
             // | K kb1 | Q kb1, 512 units each: Q for k = 2, 3, 6, 7; tile row
-            // (ts >> 3) + 32 (k & 1)), then V (k = 8..11). Four loads before
-            // their stores in each group.
+            // (ts >> 3) + 32 (k & 1)). Four loads before their stores in each
+            // group. (V is converted by the g/beta warp.)
             const float* qsc = gb_slot(m) + GB_QSC;
             const float q0 = qsc[ts >> 3], q1 = qsc[(ts >> 3) + 32];
 #pragma unroll 1
-            for (int i = 0; i < 3; ++i) {
-                uint4* base = i < 2 ? reinterpret_cast<uint4*>(kq_tile(m)) + 1024 * i : reinterpret_cast<uint4*>(v_tile(m));
+            for (int i = 0; i < 2; ++i) {
+                uint4* base = reinterpret_cast<uint4*>(kq_tile(m)) + 1024 * i;
                 uint4 u[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) u[j] = base[ts + 256 * j];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint4 w = u[j];
-                    if (j >= 2) {  // Q (i < 2) times gamma scale
-                        const float f = i < 2 ? (j == 2 ? q0 : q1) : 1.f;
+                    if (j >= 2) {  // Q times gamma scale
+                        const float f = j == 2 ? q0 : q1;
                         const float2 a = unbf2(w.x), b2 = unbf2(w.y), c = unbf2(w.z), d = unbf2(w.w);
                         w.x = h2(a.x * f, a.y * f); w.y = h2(b2.x * f, b2.y * f);
                         w.z = h2(c.x * f, c.y * f); w.w = h2(d.x * f, d.y * f);
