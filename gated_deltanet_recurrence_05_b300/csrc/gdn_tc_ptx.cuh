@@ -62,33 +62,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait with an explicit suspend-time hint: the thread may sleep up to
-// `hint_ns` waiting for the phase instead of returning at once.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Bounded wait for phase `parity` of `bar`. Each try_wait may suspend the
-// thread for up to `hint_ns` until the phase completes (the hardware wakes it
-// at completion), so waiting costs no issue slots. Gives up (returns false)
-// after `max_polls` polls (about max_polls x hint_ns of wall time at most), or
-// as soon as *abort becomes nonzero; on giving up it raises *abort so that
-// every other waiter also gives up. `abort` may be null (teardown waits that
-// must not be cut short by an abort). The loop is kept small: it is inlined at
-// every wait site and the kernel's instruction footprint matters.
+// thread until the phase completes or a system-dependent time limit passes
+// (no suspend-time hint: an explicit hint of tens of microseconds measured
+// about 1% slower on the tensor-core prefill), so waiting costs few issue
+// slots. Gives up (returns false) after `max_polls` polls, or as soon as
+// *abort becomes nonzero; on giving up it raises *abort so that every other
+// waiter also gives up. `abort` may be null (teardown waits that must not be
+// cut short by an abort). The loop is kept small: it is inlined at every wait
+// site and the kernel's instruction footprint matters.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t max_polls = 1u << 17) {
 #pragma unroll 1
     for (uint32_t i = 0; i < max_polls; ++i) {
-        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
     }
     if (abort) *abort = 1;
