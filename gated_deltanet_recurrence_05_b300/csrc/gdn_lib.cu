@@ -113,10 +113,60 @@ gdn_status launch_decode(const void* q, const void* k, const void* v, const floa
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// The TMA-fed filter (gdn::short_conv_tma_kernel) when the input is 16-byte
+// aligned and whole 512-byte channel blocks cover the channels; false when
+// the tensor map cannot be made (the caller then uses the register-tiled
+// kernel).
+template <typename T, int K>
+bool launch_short_conv_tma(const void* x, const float* w, void* y, const int32_t* cu, const float* st_in,
+                           float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s,
+                           gdn_status& st) {
+    constexpr int V = 16 / (int)sizeof(T);
+    if (C % (32 * V) != 0 || (ng != 0 && ng < V) || (reinterpret_cast<uintptr_t>(x) & 15u) != 0 || total <= 0 ||
+        total >= (1LL << 31))
+        return false;
+    auto enc = gdn::tensor_map_encoder();
+    if (enc == nullptr) return false;
+    CUtensorMap map;
+    cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)total};
+    cuuint64_t strides[1] = {(cuuint64_t)C * sizeof(T)};
+    cuuint32_t box[2] = {(cuuint32_t)(32 * V), (cuuint32_t)(gdn::pro::TILE + K - 1)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&map, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    auto kern = ng == 0 ? gdn::short_conv_tma_kernel<T, K, 0>
+                        : ng == 128 ? gdn::short_conv_tma_kernel<T, K, 128> : gdn::short_conv_tma_kernel<T, K, -1>;
+    const int smem = (int)gdn::pro::smem_bytes<K>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+    const DevInfo di = dev_info();
+    const long long ncb = C / (32 * V);
+    const long long ntt = (total + gdn::pro::TILE - 1) / gdn::pro::TILE;
+    // persistent: two CTAs per SM, a multiple of the channel blocks
+    const long long per_cb = std::max(1LL, std::min(ntt, 2LL * std::max(di.sms, 1) / ncb));
+    if (ncb * per_cb > 0x7fffffffLL) return false;
+    const long long eq = cu ? 0 : total / N;
+    kern<<<(unsigned)(ncb * per_cb), 256, smem, s>>>(map, static_cast<const T*>(x), w, static_cast<T*>(y), cu, st_in,
+                                                     st_out, N, total, eq, C, ng, eps, 1u << 17);
+    st = cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    return true;
+}
+
 template <typename T, int K>
 gdn_status launch_short_conv(const void* x, const float* w, void* y, const int32_t* cu, const float* st_in,
                              float* st_out, int N, long long total, int C, int ng, float eps, cudaStream_t s) {
     const DevInfo di = dev_info();
+    gdn_status tst = GDN_OK;
+    if (launch_short_conv_tma<T, K>(x, w, y, cu, st_in, st_out, N, total, C, ng, eps, s, tst)) {
+        if (tst != GDN_OK) return tst;
+        if (st_out && (cu || total == 0) && K > 1) {  // empty sequences carry their state over
+            const long long n = (long long)N * C * (K - 1);
+            gdn::conv_state_carry_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(cu, st_in, st_out, N,
+                                                                                      (long long)C * (K - 1));
+        }
+        return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
     const long long runs = (total + 7) / 8;  // tiles of 8 tokens, one per warp
     // 8 channels per lane when the channels and the head size allow it
     const bool v8 = C % 256 == 0 && (ng == 0 || ng >= 8);

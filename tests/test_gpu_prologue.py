@@ -89,6 +89,45 @@ def test_short_conv_prefill_shapes():
             assert_parity(y[r:r + 1].float().numpy(), yr[-1:], TAU_F32, f"y[{r}]", out_bf16=True)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("ng", [0, 128])
+def test_short_conv_many_tiles_two_channel_blocks(dtype, ng):
+    """Sequences that span several 64-token tiles of the TMA-fed kernel and
+    start or end inside a tile (and inside one warp's 8 tokens), two channel
+    blocks, conv states in and out: every output and state element against
+    the oracle."""
+    lengths = [130, 1, 200, 0, 64, 65, 7]
+    C = 512 if dtype == "bf16" else 256
+    x, w, s0, cu = _case(lengths, C, 4, dtype, seed=77 + ng)
+    y, fs = gdn.short_conv(x.cuda(), w.cuda(), cu_seqlens=cu.cuda(), conv_state=s0.cuda(), return_final_state=True,
+                           norm_group=ng)
+    assert gdn.get_device_error() == 0
+    y_ref, fs_ref = oracle.short_conv(x, w, cu_seqlens=cu.numpy(), state0=s0, norm_group=ng)
+    assert_parity(y.float().cpu().numpy(), y_ref, TAU_F32, "y", out_bf16=(dtype == "bf16"))
+    np.testing.assert_array_equal(fs.cpu().numpy(), fs_ref.astype(np.float32))
+
+
+def test_short_conv_tma_and_register_kernels_agree():
+    """bf16 with 256 channels goes through the TMA-fed kernel (whole 512-byte
+    channel blocks); each half of 128 channels alone goes through the
+    register-tiled kernel. Both evaluate every token with the same code, so
+    with heads of 128 channels the outputs and states are bit-identical."""
+    lengths = [100, 37, 3, 70]
+    x, w, s0, cu = _case(lengths, 256, 4, "bf16", seed=91)
+    xc, wc, s0c, cuc = x.cuda(), w.cuda(), s0.cuda(), cu.cuda()
+    y, fs = gdn.short_conv(xc, wc, cu_seqlens=cuc, conv_state=s0c, return_final_state=True, norm_group=128)
+    for h in range(2):
+        sl = slice(128 * h, 128 * (h + 1))
+        yh, fsh = gdn.short_conv(xc[:, sl].contiguous(), wc[sl].contiguous(), cu_seqlens=cuc,
+                                 conv_state=s0c[:, sl].contiguous(), return_final_state=True, norm_group=128)
+        assert gdn.get_device_error() == 0
+        np.testing.assert_array_equal(yh.float().cpu().numpy(), y[:, sl].float().cpu().numpy())
+        np.testing.assert_array_equal(fsh.cpu().numpy(), fs[:, sl].cpu().numpy())
+    y_ref, fs_ref = oracle.short_conv(x, w, cu_seqlens=cu.numpy(), state0=s0, norm_group=128)
+    assert_parity(y.float().cpu().numpy(), y_ref, TAU_F32, "y", out_bf16=True)
+    np.testing.assert_array_equal(fs.cpu().numpy(), fs_ref.astype(np.float32))
+
+
 def test_short_conv_rejects_bad_seqlens_on_device():
     """A cu_seqlens entry past the end of the tokens is caught by the kernel's
     own check before any access: the affected run is skipped and the error bit
