@@ -298,8 +298,9 @@ gdn_status gdn_decode_step_gated(const void* q, const void* k, const void* v,
  *                 dividing C
  * C               a multiple of 4; x and y 16-byte aligned
  *
- * One warp per (token, 128 channels), one read of x from DRAM and one write
- * of y. Errors as for gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG for y == x.
+ * One read of x from DRAM and one write of y (tiles of 64 tokens moved by TMA
+ * when C is a multiple of 256 bf16 / 128 fp32 channels, else a register-tiled
+ * kernel). Errors as for gdn_chunk_fwd, plus GDN_ERR_INVALID_ARG for y == x.
  */
 gdn_status gdn_short_conv(const void* x, const float* w, void* y, const int32_t* cu_seqlens,
                           const float* conv_state_in, float* conv_state_out, int32_t num_seqs,
