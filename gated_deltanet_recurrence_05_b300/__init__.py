@@ -27,13 +27,14 @@ import torch
 
 __all__ = ["chunk_fwd", "decode_step", "plan_seq_order", "get_device_error", "lib",
            "GdnError", "LIB_PATH", "F32", "BF16", "FLAG_FORCE_SIMT", "FLAG_TEST_WAIT_TIMEOUT", "FLAG_NO_SPLIT",
-           "DEVERR_SEQLENS", "DEVERR_TIMEOUT", "DEVERR_RANGE"]
+           "FLAG_BALANCE", "DEVERR_SEQLENS", "DEVERR_TIMEOUT", "DEVERR_RANGE"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgdn.so")
 F32, BF16 = 0, 1
 FLAG_FORCE_SIMT = 1
 FLAG_TEST_WAIT_TIMEOUT = 2   # failure-path tests only (see include/gdn.h)
 FLAG_NO_SPLIT = 4            # one CTA per (sequence, value head): no sequence segments
+FLAG_BALANCE = 8             # balanced shares of chunks for any equal-length batch (tests of the share logic)
 DEVERR_SEQLENS, DEVERR_TIMEOUT, DEVERR_RANGE = 1, 2, 4
 _STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_CUDA",
            4: "GDN_ERR_TIMEOUT"}
@@ -159,7 +160,7 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
               scale: float = 0.0, chunk_size: int = 0, output_final_state: bool = True,
               out: Optional[torch.Tensor] = None, final_state_out: Optional[torch.Tensor] = None,
               force_simt: bool = False, test_wait_timeout: bool = False, split: bool = True,
-              gate: Optional[torch.Tensor] = None, norm_weight: Optional[torch.Tensor] = None,
+              balance: bool = False, gate: Optional[torch.Tensor] = None, norm_weight: Optional[torch.Tensor] = None,
               eps: float = 1e-6, stream=None):
     """Prefill of the recurrence over packed tokens (see include/gdn.h).
 
@@ -195,7 +196,7 @@ def chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor
         fs = final_state_out if final_state_out is not None else torch.empty(
             (N, h_v, d_k, d_v), dtype=torch.float32, device=v.device)
     flags = ((FLAG_FORCE_SIMT if force_simt else 0) | (FLAG_TEST_WAIT_TIMEOUT if test_wait_timeout else 0) |
-             (0 if split else FLAG_NO_SPLIT))
+             (0 if split else FLAG_NO_SPLIT) | (FLAG_BALANCE if balance else 0))
     if gate is None:
         if norm_weight is not None:
             raise ValueError("norm_weight needs a gate")

@@ -74,6 +74,16 @@ struct TcArgs {
     uint32_t max_polls;    // poll limit of every mbarrier wait
     int withhold_chunk;    // test of the failure path: the g/beta arrival of this chunk is never made (-1: none)
     int nseg;              // segments per sequence (one CTA each; 1 = the whole sequence in one CTA)
+    int bal_chunks;        // > 0: equal-length sequences, every CTA takes this many consecutive chunks of
+                           // the (sequence, head) units in order (at most two pieces of units); nseg = 1
+};
+
+// A CTA's piece of a (sequence, value head) unit: it stores the outputs of
+// tokens [seg_a, t1) and processes tokens [t0, t1), t0 <= seg_a (a prefix
+// started from a zero state, or the sequence start s0 with the initial state)
+struct Piece {
+    long long t0, seg_a, t1, s0;
+    int h, hk, n_seq, nc, len, from_start, last_seg, pad;
 };
 
 namespace tck {
@@ -111,7 +121,8 @@ constexpr uint32_t GB_SLOT_BYTES = GB_FLOATS * 4;
 constexpr uint32_t OFF_BAR = OFF_GB + GB_SLOTS * GB_SLOT_BYTES;
 constexpr uint32_t NUM_BARS = 40;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;    // + alignment slack
+constexpr uint32_t OFF_PIECES = OFF_MISC + 16;          // two Piece records
+constexpr uint32_t SMEM_BYTES = OFF_PIECES + 2 * 64 + 1024;  // + alignment slack
 static_assert(OFF_WT % 1024 == 0 && OFF_BW % 1024 == 0 && OFF_P % 1024 == 0 && OFF_AS % 1024 == 0,
               "tile alignment");
 static_assert(GB_SLOT_BYTES % 16 == 0 && OFF_GB % 16 == 0, "gb slot alignment");
@@ -266,10 +277,11 @@ __device__ __forceinline__ void solve_block_row(int bi, uint32_t as_u, uint32_t 
     }
 }
 
-// A/P pass of the prep warps on chunk n (the A and Ad tiles and P buffer
-// n & 1): from X = [K; Q] K^T in TMEM, row r of A (rows 0-63, TMEM lanes
-// 0-63) or of P (lanes 64-127) per thread; gt = the thread's TMEM lane.
-__device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float* gb, int n, int len, float scale,
+// A/P pass of the prep warps on chunk n of the CTA (the A and Ad tiles and P
+// buffer n & 1; `rows` of its rows are tokens): from X = [K; Q] K^T in TMEM,
+// row r of A (rows 0-63, TMEM lanes 0-63) or of P (lanes 64-127) per thread;
+// gt = the thread's TMEM lane.
+__device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float* gb, int n, int rows, float scale,
                                         int gt, unsigned long long* tb_) {
     using namespace tc;
     const int wq = gt >> 5;
@@ -286,7 +298,7 @@ __device__ __forceinline__ void ap_pass(uint8_t* sm, uint32_t tmem, const float*
         // beta_r and the output scale enter as exponent offsets (log2 of 0 is -inf: row of zeros)
         const float base = gb[GB_G + r] + (isA ? lg2(gb[GB_BET + r]) : lg2(scale));
         // kept columns: s < r (A), s <= r on live rows (P)
-        const int lim = isA ? r : (r < min(C, len - n * C) ? r + 1 : 0);
+        const int lim = isA ? r : (r < rows ? r + 1 : 0);
         uint8_t* row = isA ? As + r * 128 : sm + OFF_P + (uint32_t)grp * 8192 + r * 128;
         const bool wide = (wq & 1) != 0;  // rows 32-63
         // quarters of 16 columns (rows 0-31 need only 0-31); rows 32-63 take
@@ -401,26 +413,68 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + OFF_MISC);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + OFF_MISC + 4);
 
-    // ---- unit of work: (sequence, value head, segment of the sequence). A
-    //      segment stores the outputs of tokens [seg_a, t1); it starts from a zero
-    //      state a few tokens earlier (segment_prefix_start), or from the
-    //      sequence's initial state at its first token
-    const int seg = blockIdx.x % p.nseg;
-    const int h = (blockIdx.x / p.nseg) % p.h_v;
-    const int pos = blockIdx.x / p.nseg / p.h_v;
-    int n_seq;
-    if (!seq_of(p.order, pos, p.num_seqs, n_seq)) return;
-    long long s0, s1;  // the sequence's tokens
-    if (!seq_bounds(p.cu, n_seq, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
-    const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + C - 1) / C * C;
-    const long long seg_a = s0 + seg * seg_len;
-    if (seg > 0 && seg_a >= s1) return;  // an empty segment
-    const long long t1 = seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1;
-    const int hk = h / p.grp;
+    // ---- work of this CTA: one or two pieces of (sequence, value head) units.
+    //      A piece stores the outputs of tokens [seg_a, t1); it starts from a
+    //      zero state a few tokens earlier (segment_prefix_start), or from the
+    //      sequence's initial state at its first token. Either a segment of a
+    //      unit (nseg segments per sequence), or, with bal_chunks, the CTA's
+    //      share of the chunks of all units taken in order (equal lengths: a
+    //      share ends at most one unit after the one it starts in).
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Piece* pieces = reinterpret_cast<Piece*>(sm + OFF_PIECES);
+    // (seq_a: first stored token, t1: end, s0, s1: the sequence, h: value head)
+    struct Spec { long long seg_a, t1, s0, s1; int h, n_seq; };
+    Spec sp0{}, sp1{};
+    int npieces = 0;
+    if (p.bal_chunks == 0) {
+        const int seg = blockIdx.x % p.nseg;
+        const int h = (blockIdx.x / p.nseg) % p.h_v;
+        const int pos = blockIdx.x / p.nseg / p.h_v;
+        int n_seq;
+        if (!seq_of(p.order, pos, p.num_seqs, n_seq)) return;
+        long long s0, s1;  // the sequence's tokens
+        if (!seq_bounds(p.cu, n_seq, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+        const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + C - 1) / C * C;
+        const long long seg_a = s0 + seg * seg_len;
+        if (seg > 0 && seg_a >= s1) return;  // an empty segment
+        sp0 = Spec{seg_a, seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1, s0, s1, h, n_seq};
+        npieces = 1;
+    } else {
+        const long long nch = (p.eq_len + C - 1) / C;  // chunks per unit
+        const long long ctot = (long long)p.num_seqs * p.h_v * nch;
+        long long a = (long long)blockIdx.x * p.bal_chunks;
+        const long long b = min(a + (long long)p.bal_chunks, ctot);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (a >= b) break;
+            const long long u = a / nch, c_lo = a - u * nch, c_hi = min(nch, c_lo + (b - a));
+            const int h = (int)(u % p.h_v), pos = (int)(u / p.h_v);
+            int n_seq;
+            if (!seq_of(p.order, pos, p.num_seqs, n_seq)) return;
+            long long s0, s1;
+            if (!seq_bounds(p.cu, n_seq, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+            const Spec x{s0 + c_lo * C, min(s0 + c_hi * C, s1), s0, s1, h, n_seq};
+            if (i == 0) sp0 = x; else sp1 = x;
+            ++npieces;
+            a += c_hi - c_lo;
+        }
+        if (npieces == 0) return;
+    }
     if (warp == 3) {
-        const long long ts = seg > 0 ? segment_prefix_start(p, s0, seg_a, h, hk, lane) : s0;
-        if (lane == 0) *reinterpret_cast<long long*>(sm + OFF_MISC + 8) = ts;
+        auto fill = [&](Piece& P, const Spec x) {
+            const int hk_i = x.h / p.grp;
+            const long long ts = x.seg_a > x.s0 ? segment_prefix_start(p, x.s0, x.seg_a, x.h, hk_i, lane) : x.s0;
+            if (lane == 0) {
+                P.t0 = ts; P.seg_a = x.seg_a; P.t1 = x.t1; P.s0 = x.s0;
+                P.h = x.h; P.hk = hk_i; P.n_seq = x.n_seq;
+                P.len = (int)(x.t1 - ts); P.nc = (P.len + C - 1) / C;
+                P.from_start = ts == x.s0;
+                P.last_seg = x.t1 == x.s1;  // the piece ends the sequence: it writes the final state
+                P.pad = 0;
+            }
+        };
+        fill(pieces[0], sp0);
+        if (npieces > 1) fill(pieces[1], sp1);
     }
 #ifdef GDN_TRACE
     unsigned long long* const tb_ = blockIdx.x == 0 ? g_trace : nullptr;  // traced block
@@ -466,11 +520,14 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const long long t0 = *reinterpret_cast<const long long*>(sm + OFF_MISC + 8);  // first token processed
-    const int len = (int)(t1 - t0);
-    const int nc = (len + C - 1) / C;
-    const bool from_start = t0 == s0;  // the initial state applies
-    const bool last_seg = t1 == s1;    // this CTA ends the sequence: it writes the final state
+    const int nc0 = pieces[0].nc;
+    const int nc = nc0 + (npieces > 1 ? pieces[1].nc : 0);  // chunks of the CTA
+    // the piece of the CTA's chunk m, and m's chunk index n within it
+    auto piece_of = [&](int m, int& n) -> const Piece& {
+        const int i = (npieces > 1 && m >= nc0) ? 1 : 0;
+        n = m - (i ? nc0 : 0);
+        return pieces[i];
+    };
     if (lane == 0) GDN_TRACE_AT(60, warp);
 
     auto kq_tile = [&](int n) { return sm + OFF_KQ + (uint32_t)(n % KQ_STAGES) * KQ_BYTES; };
@@ -497,8 +554,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         if (lane == 0) {
             int issued_kq = 0, issued_v = 0;
             for (int n = 0; n < nc && !*abort_flag; ++n) {
-                const int t = (int)(t0 + (long long)n * C);
-                if (n + 3 < nc) {  // warm L2 for chunk n + 3 (its stage is still in use)
+                int nl;  // chunk n's index within its piece
+                const Piece& P = piece_of(n, nl);
+                const int t = (int)(P.t0 + (long long)nl * C), hk = P.hk, h = P.h;
+                if (nl + 3 < P.nc) {  // warm L2 for chunk n + 3 of the same piece (its stage is still in use)
                     const int tp = t + 3 * C;
                     tma_prefetch_l2_3d(&mapK, 0, hk, tp); tma_prefetch_l2_3d(&mapK, 64, hk, tp);
                     tma_prefetch_l2_3d(&mapQ, 0, hk, tp); tma_prefetch_l2_3d(&mapQ, 64, hk, tp);
@@ -679,8 +738,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const int slot = n % GB_SLOTS;
             if (n >= GB_SLOTS && !WAITW(B_GB_EMPTY + slot, ((n / GB_SLOTS) - 1) & 1)) break;
             float* gb = gb_slot(n);
-            const long long t = t0 + (long long)n * C;
-            const int L = min(C, len - n * C);
+            int nl;
+            const Piece& P = piece_of(n, nl);
+            const long long t = P.t0 + (long long)nl * C;
+            const int L = min(C, P.len - nl * C), h = P.h;
             const int r0 = 2 * lane, r1 = 2 * lane + 1;
             const float g0 = r0 < L ? p.g[(t + r0) * p.h_v + h] : 0.f;
             const float g1 = r1 < L ? p.g[(t + r1) * p.h_v + h] : 0.f;
@@ -738,7 +799,9 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (named_sync_or(bar_id, 128, !ok)) break;
             if (gt == 0) GDN_TRACE_AT(0, n);
             tc_fence_after();
-            ap_pass(sm, tmem, gb, n, len, p.scale, gt, tb_);
+            int nl;
+            const Piece& P = piece_of(n, nl);
+            ap_pass(sm, tmem, gb, n, min(C, P.len - nl * C), p.scale, gt, tb_);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[B_XFREE]);
@@ -803,16 +866,37 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         const int ws = warp - 8, q4 = warp & 3, hf = ws >> 2;
         const int j = 32 * q4 + lane;
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-        const size_t sbase = ((size_t)n_seq * p.h_v + h) * (size_t)(D * D);
+        auto sbase_of = [&](const Piece& P) { return ((size_t)P.n_seq * p.h_v + P.h) * (size_t)(D * D); };
         float S[64];
-        if (p.h0 && from_start) {
-            const float* hp = p.h0 + sbase + (size_t)(64 * hf) * D + j;
+        // a piece starts from the sequence's initial state at its first token,
+        // else from zeros
+        auto load_initial = [&](const Piece& P) {
+            if (p.h0 && P.from_start) {
+                const float* hp = p.h0 + sbase_of(P) + (size_t)(64 * hf) * D + j;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) S[c] = hp[c * D];
-        } else {
+                for (int c = 0; c < 64; ++c) S[c] = hp[c * D];
+            } else {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) S[c] = 0.f;
-        }
+                for (int c = 0; c < 64; ++c) S[c] = 0.f;
+            }
+        };
+        // end of a piece: fp16 range check; the final state if the piece ends
+        // its sequence. A value beyond the range of the fp16 operands (v, the
+        // state or a chunk's errors above 65504) became an infinity in a
+        // product and has left a non-finite value in the fp32 state, where it
+        // stays (decay keeps infinities, sums keep NaNs)
+        auto finish_piece = [&](const Piece& P) {
+            bool finite = true;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) finite = finite && (fabsf(S[c]) < INFINITY);
+            if (__any_sync(0xffffffffu, !finite) && lane == 0) set_device_error(4u);
+            if (p.hT && P.last_seg) {
+                float* hp = p.hT + sbase_of(P) + (size_t)(64 * hf) * D + j;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
+            }
+        };
+        load_initial(pieces[0]);
         auto put_state_f16 = [&]() {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
@@ -955,6 +1039,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
 #pragma unroll
                     for (int c = 0; c < 32; ++c) S[32 + c] = fmaf(gC, S[32 + c], __uint_as_float(acc1[c]));
                 }
+                if (npieces > 1 && n == nc0 - 1) {  // the first piece ends: the second one's initial state
+                    finish_piece(pieces[0]);
+                    load_initial(pieces[1]);
+                }
                 put_state_f16();
                 tc_fence_before();
                 __syncwarp();
@@ -967,13 +1055,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
                 if (!WAITW(B_OREADY, n & 1)) break;
                 tc_fence_after();
                 {
-                    // o[t0 + n C + r][h][j] for r < nv: one row per register, through a
+                    // o[t0 + nl C + r][h][j] for r < nv: one row per register, through a
                     // byte pointer stepped by the token stride
-                    const int nv = min(C, len - n * C) - 32 * hf;  // valid rows of this half
-                    // rows before token seg_a belong to the segment's prefix: not stored
-                    const long long r0 = t0 + (long long)n * C + 32 * hf;
-                    const int nskip = seg_a > r0 ? (int)min(32LL, seg_a - r0) : 0;
-                    char* orow = reinterpret_cast<char*>(o + ((size_t)(t0 + (long long)n * C + 32 * hf) * p.h_v + h) * D + j);
+                    int nl;
+                    const Piece& P = piece_of(n, nl);
+                    const int nv = min(C, P.len - nl * C) - 32 * hf;  // valid rows of this half
+                    // rows before token seg_a belong to the piece's prefix: not stored
+                    const long long r0 = P.t0 + (long long)nl * C + 32 * hf;
+                    const int nskip = P.seg_a > r0 ? (int)min(32LL, P.seg_a - r0) : 0;
+                    char* orow = reinterpret_cast<char*>(o + ((size_t)r0 * p.h_v + P.h) * D + j);
                     const size_t ostep = (size_t)p.h_v * D * sizeof(TOut);
                     uint32_t ov[32];
                     tmem_ld32(tmem + lane_base + T_O + 32 * hf, ov);
@@ -992,21 +1082,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             if (n + 2 < nc && !convert(n + 2)) break;
             if (n >= 0 && ws == 0 && lane == 0) GDN_TRACE_AT(14, n);
         }
-        if (!*abort_flag) {
-            // fp16 range: a value beyond the range of the fp16 operands (v, the
-            // state or a chunk's errors above 65504) became an infinity in a
-            // product and has left a non-finite value in the fp32 state, where
-            // it stays (decay keeps infinities, sums keep NaNs)
-            bool finite = true;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) finite = finite && (fabsf(S[c]) < INFINITY);
-            if (__any_sync(0xffffffffu, !finite) && lane == 0) set_device_error(4u);
-            if (p.hT && last_seg) {
-                float* hp = p.hT + sbase + (size_t)(64 * hf) * D + j;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) hp[c * D] = S[c];
-            }
-        }
+        if (!*abort_flag) finish_piece(pieces[npieces - 1]);
     }
 
     // ---- teardown (also after an abort): the producer has drained its TMA
@@ -1065,7 +1141,9 @@ inline gdn_status launch_tc(const TcArgs& a, bool out_bf16, cudaStream_t s) {
     if (!make_head_map(&mq, a.q, a.total, a.h_qk) || !make_head_map(&mk, a.k, a.total, a.h_qk) ||
         !make_head_map(&mv, a.v, a.total, a.h_v))
         return GDN_ERR_CUDA;
-    const long long blocks = (long long)a.num_seqs * a.h_v * a.nseg;
+    const long long ctot = (long long)a.num_seqs * a.h_v * ((a.eq_len + tck::C - 1) / tck::C);
+    const long long blocks =
+        a.bal_chunks > 0 ? (ctot + a.bal_chunks - 1) / a.bal_chunks : (long long)a.num_seqs * a.h_v * a.nseg;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     if (out_bf16) {
         auto kern = tck::chunk_tc_kernel<__nv_bfloat16>;

@@ -592,7 +592,8 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         return GDN_ERR_INVALID_ARG;
     if (!ok_dtype(dtype_qkv) || !ok_dtype(dtype_o)) return GDN_ERR_INVALID_ARG;
     if (chunk_size != 0 && chunk_size != 16 && chunk_size != 32 && chunk_size != 64) return GDN_ERR_INVALID_ARG;
-    if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT | GDN_FLAG_NO_SPLIT)) return GDN_ERR_INVALID_ARG;
+    if (flags & ~(GDN_FLAG_FORCE_SIMT | GDN_FLAG_TEST_WAIT_TIMEOUT | GDN_FLAG_NO_SPLIT | GDN_FLAG_BALANCE))
+        return GDN_ERR_INVALID_ARG;
     if (gate && (!(eps >= 0.f) || !isfinite(eps))) return GDN_ERR_INVALID_ARG;
     if (d_k > 128 || d_v > 128) return GDN_ERR_UNSUPPORTED;
     if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
@@ -621,18 +622,33 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         const bool stall = (flags & GDN_FLAG_TEST_WAIT_TIMEOUT) != 0;
         a.max_polls = stall ? (1u << 12) : (1u << 17);
         a.withhold_chunk = stall ? 1 : -1;
-        // Fewer (sequence, head) units than SMs: split each sequence into
-        // segments of at least 512 tokens, one CTA each (the kernel starts a
-        // segment from a zero state where the decay has made the earlier
-        // tokens' influence negligible, else from the sequence start). Not
-        // when the final state overwrites the initial state: a later segment
-        // could then finish before an earlier one has read it.
+        // Fewer (sequence, head) units than SMs: split the work of a unit over
+        // several CTAs (the kernel starts a piece of a unit from a zero state
+        // where the decay has made the earlier tokens' influence negligible,
+        // else from the sequence start). Equal lengths with at least 128
+        // chunks per SM: every CTA takes the same number of consecutive chunks
+        // of the units in order, so that all SMs share the work evenly (with
+        // fewer, a piece's fixed costs, the prefix search at the start and
+        // the state hand-over between two units, outweigh the balance: it
+        // measured slower on 4 x 4096 tokens). Otherwise segments of at least
+        // 512 tokens, one CTA each, up to SMs / units per sequence. Not when
+        // the final state overwrites the initial state: a later piece could
+        // then finish before an earlier one has read it.
         a.nseg = 1;
+        a.bal_chunks = 0;
         if (!(flags & GDN_FLAG_NO_SPLIT) && !(final_state != nullptr && final_state == initial_state)) {
             const long long units = (long long)num_seqs * h_v, sms = std::max(dev_info().sms, 1);
             if (units < sms) {
-                const long long by_len = (long long)(total_tokens / num_seqs) / 512;
-                a.nseg = (int)std::max(1LL, std::min(std::min(sms / units, by_len), 64LL));
+                const long long nch = (eq_len + gdn::tck::C - 1) / gdn::tck::C;
+                const long long share = (units * nch + sms - 1) / sms;
+                const bool force = (flags & GDN_FLAG_BALANCE) != 0;
+                const long long sh = force ? std::max(share, 3LL) : share;
+                if (cu_seqlens == nullptr && (force || share >= 128) && sh < nch && sh <= 0x7fffffffLL) {
+                    a.bal_chunks = (int)sh;
+                } else {
+                    const long long by_len = (long long)(total_tokens / num_seqs) / 512;
+                    a.nseg = (int)std::max(1LL, std::min(std::min(sms / units, by_len), 64LL));
+                }
             }
         }
         const gdn_status st = gdn::launch_tc(a, bf_out, s);

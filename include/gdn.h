@@ -76,9 +76,14 @@ enum {
                                   final states are undefined after such a call;
                                   the stream stays usable. No effect on the
                                   CUDA-core kernel. */,
-    GDN_FLAG_NO_SPLIT = 4      /* keep every sequence in one CTA per value head
+    GDN_FLAG_NO_SPLIT = 4,     /* keep every sequence in one CTA per value head
                                   on the tensor-core path (see gdn_chunk_fwd:
                                   sequence segments) */
+    GDN_FLAG_BALANCE = 8       /* equal-length sequences (cu_seqlens NULL) with
+                                  fewer (sequence, head) units than SMs: use
+                                  balanced shares of at least 3 chunks whatever
+                                  the length (by default only from 128 chunks
+                                  per SM on; for tests of the share logic) */
 };
 
 /* Device error codes (bit set) returned by gdn_get_device_error. */
@@ -123,15 +128,19 @@ enum {
  * Sequence segments (tensor-core path): when there are fewer (sequence,
  * value head) units than SMs, each sequence is split into up to SMs / units
  * segments of at least 512 tokens, one CTA each, unless GDN_FLAG_NO_SPLIT is
- * given or final_state == initial_state. A later segment starts from a zero
+ * given or final_state == initial_state. Equal-length sequences with at least
+ * 128 chunks of 64 tokens per SM (or GDN_FLAG_BALANCE) are instead cut into
+ * balanced shares: CTA i takes chunks [i L, (i + 1) L) of all units in order,
+ * L = ceil(chunks / SMs), i.e. the end of one unit and the start of the next
+ * (pieces). A piece that does not begin its sequence starts from a zero
  * state at the nearest earlier token ts for which the product of
  * alpha_t max(1, |1 - beta_t |k_t|^2|) over tokens ts .. (its first token - 1)
  * is below 2^-40: each token maps a difference of states D to
  * alpha_t (I - beta_t k_t k_t^T) D, whose spectral norm that factor bounds,
- * so the state at the segment's start then differs from the exact one by
+ * so the state at the piece's start then differs from the exact one by
  * at most 2^-40 times the spectral norm of the true state before ts (far
  * below fp32 rounding). Where the product never gets that small (alpha = 1,
- * slow decay over a short sequence) the segment starts from the sequence's
+ * slow decay over a short sequence) the piece starts from the sequence's
  * first token and initial state, which is exact.
  * Returns GDN_ERR_INVALID_ARG for null/misaligned pointers, H_v % H_qk != 0,
  * N < 0, T_total < 0, T_total % N != 0 without cu_seqlens, or bad codes;

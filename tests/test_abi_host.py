@@ -91,7 +91,7 @@ def _fwd(L, **kw):
     (dict(dq=7), INVALID),
     (dict(do=2), INVALID),
     (dict(chunk=48), INVALID),
-    (dict(flags=8), INVALID),
+    (dict(flags=32), INVALID),
     (dict(flags=2 | 16), INVALID),               # only documented flag bits
     (dict(d_k=256), UNSUPPORTED),
     (dict(d_v=129), UNSUPPORTED),

@@ -323,6 +323,42 @@ def test_sequence_segments_match_oracle(k_scale):
     assert_parity(S, S2, TAU_BF16, "final state vs unsplit")
 
 
+def _run_batch(d, N, **kw):
+    dd = to_cuda(d)
+    o, S = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], None, num_seqs=N,
+                         output_dtype=torch.float32, **kw)
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    return o.cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("g_zero", [False, True])
+def test_balanced_shares_match_oracle(g_zero):
+    """Equal-length batch cut into balanced shares of 3 chunks (GDN_FLAG_BALANCE):
+    16 chunks per unit, so most CTAs take the end of one (sequence, head) unit
+    and the start of the next, the first piece started from a zero state after
+    its prefix. Every output and final state against the oracle and the
+    unsplit kernel; with alpha = 1 every piece restarts at its sequence start
+    and the results equal the unsplit kernel's bit for bit."""
+    N, L = 2, 1000
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16", batch=N, seqlen=L, h0_std=0.02,
+                                seed=64)
+    assert d["cu_seqlens"] is None
+    if g_zero:
+        d["g"].zero_()
+    o, S = _run_batch(d, N, balance=True)
+    o2, S2 = _run_batch(d, N, split=False)
+    if g_zero:
+        np.testing.assert_array_equal(o, o2)
+        np.testing.assert_array_equal(S, S2)
+    else:
+        o_ref, S_ref = _ref(d)
+        assert_parity(o, o_ref, TAU_BF16, "o")
+        assert_parity(S, S_ref, TAU_BF16, "final state")
+        assert_parity(o, o2, TAU_BF16, "o vs unsplit")
+        assert_parity(S, S2, TAU_BF16, "final state vs unsplit")
+
+
 def test_bf16_output_segments_and_unaligned_buffer():
     """bf16 outputs with sequence segments (the rows of a segment's prefix are
     not stored) into a 16-byte aligned and a 2-byte aligned buffer: both
