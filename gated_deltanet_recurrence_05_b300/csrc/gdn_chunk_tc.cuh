@@ -74,8 +74,9 @@ struct TcArgs {
     uint32_t max_polls;    // poll limit of every mbarrier wait
     int withhold_chunk;    // test of the failure path: the g/beta arrival of this chunk is never made (-1: none)
     int nseg;              // segments per sequence (one CTA each; 1 = the whole sequence in one CTA)
-    int bal_chunks;        // > 0: equal-length sequences, every CTA takes this many consecutive chunks of
-                           // the (sequence, head) units in order (at most two pieces of units); nseg = 1
+    int bal_chunks;        // > 0: equal-length sequences, every grp CTAs take this many consecutive chunks of
+                           // the (sequence, q/k head) groups in order, one CTA per value head of the group
+                           // (at most two pieces of units each); nseg = 1
 };
 
 // A CTA's piece of a (sequence, value head) unit: it stores the outputs of
@@ -440,15 +441,19 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
         sp0 = Spec{seg_a, seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1, s0, s1, h, n_seq};
         npieces = 1;
     } else {
+        // shares of the chunks of the (sequence, q/k head) groups in order; the
+        // grp value heads of a group take the same share in grp neighbouring
+        // CTAs, so that they read the group's q and k tiles at the same time
         const long long nch = (p.eq_len + C - 1) / C;  // chunks per unit
-        const long long ctot = (long long)p.num_seqs * p.h_v * nch;
-        long long a = (long long)blockIdx.x * p.bal_chunks;
+        const long long ctot = (long long)p.num_seqs * p.h_qk * nch;
+        const int r = blockIdx.x % p.grp;  // value head within the group
+        long long a = (long long)(blockIdx.x / p.grp) * p.bal_chunks;
         const long long b = min(a + (long long)p.bal_chunks, ctot);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             if (a >= b) break;
             const long long u = a / nch, c_lo = a - u * nch, c_hi = min(nch, c_lo + (b - a));
-            const int h = (int)(u % p.h_v), pos = (int)(u / p.h_v);
+            const int h = (int)(u % p.h_qk) * p.grp + r, pos = (int)(u / p.h_qk);
             int n_seq;
             if (!seq_of(p.order, pos, p.num_seqs, n_seq)) return;
             long long s0, s1;
@@ -1141,9 +1146,9 @@ inline gdn_status launch_tc(const TcArgs& a, bool out_bf16, cudaStream_t s) {
     if (!make_head_map(&mq, a.q, a.total, a.h_qk) || !make_head_map(&mk, a.k, a.total, a.h_qk) ||
         !make_head_map(&mv, a.v, a.total, a.h_v))
         return GDN_ERR_CUDA;
-    const long long ctot = (long long)a.num_seqs * a.h_v * ((a.eq_len + tck::C - 1) / tck::C);
-    const long long blocks =
-        a.bal_chunks > 0 ? (ctot + a.bal_chunks - 1) / a.bal_chunks : (long long)a.num_seqs * a.h_v * a.nseg;
+    const long long ctot = (long long)a.num_seqs * a.h_qk * ((a.eq_len + tck::C - 1) / tck::C);  // group chunks
+    const long long blocks = a.bal_chunks > 0 ? (ctot + a.bal_chunks - 1) / a.bal_chunks * a.grp
+                                              : (long long)a.num_seqs * a.h_v * a.nseg;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     if (out_bf16) {
         auto kern = tck::chunk_tc_kernel<__nv_bfloat16>;

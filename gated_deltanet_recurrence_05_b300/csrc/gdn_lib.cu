@@ -625,13 +625,15 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         // Fewer (sequence, head) units than SMs: split the work of a unit over
         // several CTAs (the kernel starts a piece of a unit from a zero state
         // where the decay has made the earlier tokens' influence negligible,
-        // else from the sequence start). Equal lengths with at least 128
-        // chunks per SM: every CTA takes the same number of consecutive chunks
-        // of the units in order, so that all SMs share the work evenly (with
-        // fewer, a piece's fixed costs, the prefix search at the start and
-        // the state hand-over between two units, outweigh the balance: it
-        // measured slower on 4 x 4096 tokens). Otherwise segments of at least
-        // 512 tokens, one CTA each, up to SMs / units per sequence. Not when
+        // else from the sequence start). Equal lengths with shares of at least
+        // 32 chunks: the chunks of the (sequence, q/k head) groups are cut into
+        // equal shares in order, each taken by the group's grp value heads in
+        // grp neighbouring CTAs (they read the same q and k tiles at the same
+        // time), so that all SMs share the work evenly (below 32 chunks a
+        // piece's fixed costs, the prefix search at the start and the state
+        // hand-over between two units, outweigh the balance). Otherwise
+        // segments of at least 512 tokens, one CTA each, up to SMs / units
+        // per sequence. Not when
         // the final state overwrites the initial state: a later piece could
         // then finish before an earlier one has read it.
         a.nseg = 1;
@@ -639,11 +641,13 @@ gdn_status chunk_fwd_impl(const void* q, const void* k, const void* v, const flo
         if (!(flags & GDN_FLAG_NO_SPLIT) && !(final_state != nullptr && final_state == initial_state)) {
             const long long units = (long long)num_seqs * h_v, sms = std::max(dev_info().sms, 1);
             if (units < sms) {
-                const long long nch = (eq_len + gdn::tck::C - 1) / gdn::tck::C;
-                const long long share = (units * nch + sms - 1) / sms;
+                const long long nch = (eq_len + gdn::tck::C - 1) / gdn::tck::C, grp = h_v / h_qk;
+                // shares of the (sequence, q/k head) groups' chunks; grp CTAs each
+                const long long slots = std::max(1LL, sms / grp);
+                const long long share = ((long long)num_seqs * h_qk * nch + slots - 1) / slots;
                 const bool force = (flags & GDN_FLAG_BALANCE) != 0;
                 const long long sh = force ? std::max(share, 3LL) : share;
-                if (cu_seqlens == nullptr && (force || share >= 128) && sh < nch && sh <= 0x7fffffffLL) {
+                if (cu_seqlens == nullptr && (force || share >= 32) && sh < nch && sh <= 0x7fffffffLL) {
                     a.bal_chunks = (int)sh;
                 } else {
                     const long long by_len = (long long)(total_tokens / num_seqs) / 512;

@@ -82,8 +82,8 @@ enum {
     GDN_FLAG_BALANCE = 8       /* equal-length sequences (cu_seqlens NULL) with
                                   fewer (sequence, head) units than SMs: use
                                   balanced shares of at least 3 chunks whatever
-                                  the length (by default only from 128 chunks
-                                  per SM on; for tests of the share logic) */
+                                  the length (by default only from 32 chunks
+                                  per share on; for tests of the share logic) */
 };
 
 /* Device error codes (bit set) returned by gdn_get_device_error. */
@@ -128,10 +128,12 @@ enum {
  * Sequence segments (tensor-core path): when there are fewer (sequence,
  * value head) units than SMs, each sequence is split into up to SMs / units
  * segments of at least 512 tokens, one CTA each, unless GDN_FLAG_NO_SPLIT is
- * given or final_state == initial_state. Equal-length sequences with at least
- * 128 chunks of 64 tokens per SM (or GDN_FLAG_BALANCE) are instead cut into
- * balanced shares: CTA i takes chunks [i L, (i + 1) L) of all units in order,
- * L = ceil(chunks / SMs), i.e. the end of one unit and the start of the next
+ * given or final_state == initial_state. Equal-length sequences whose work
+ * comes to at least 32 chunks of 64 tokens per SM (or GDN_FLAG_BALANCE) are
+ * instead cut into balanced shares: the chunks of the (sequence, q/k head)
+ * groups, taken in order, are cut every L = ceil(chunks / (SMs / grp))
+ * chunks, and each share is processed by grp CTAs, one per value head of the
+ * group (grp = H_v / H_qk): the end of one unit and the start of the next
  * (pieces). A piece that does not begin its sequence starts from a zero
  * state at the nearest earlier token ts for which the product of
  * alpha_t max(1, |1 - beta_t |k_t|^2|) over tokens ts .. (its first token - 1)
