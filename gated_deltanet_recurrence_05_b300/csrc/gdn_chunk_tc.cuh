@@ -373,20 +373,24 @@ __device__ __forceinline__ long long segment_prefix_start(const TcArgs& p, long 
         const bool valid = tok >= s0;
         float c = 0.f;
         if (valid) {
+            // all loads of the token in flight together (one memory round trip)
+            const float gt = p.g[(size_t)tok * p.h_v + h], bt = p.beta[(size_t)tok * p.h_v + h];
             const uint4* kp = reinterpret_cast<const uint4*>(kb + ((size_t)tok * p.h_qk + hk) * D);
+            uint4 u[D / 8];
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) u[i] = kp[i];
             float ss = 0.f;
-#pragma unroll 4
+#pragma unroll
             for (int i = 0; i < D / 8; ++i) {
-                const uint4 u = kp[i];
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
                     ss = fmaf(lo, lo, fmaf(hi, hi, ss));
                 }
             }
-            const float f = fabsf(1.f - p.beta[(size_t)tok * p.h_v + h] * ss);
-            c = p.g[(size_t)tok * p.h_v + h] + (f > 1.f ? logf(f) : 0.f);
+            const float f = fabsf(1.f - bt * ss);
+            c = gt + (f > 1.f ? logf(f) : 0.f);
         }
         float incl = c;  // sum over tokens p0 - 1 .. tok
 #pragma unroll
