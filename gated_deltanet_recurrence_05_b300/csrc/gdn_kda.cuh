@@ -137,6 +137,9 @@ struct Args {
     int num_seqs, h_qk, h_v, grp;
     float scale;
     int nseg;          // segments per sequence (one CTA each; 1 = the whole sequence)
+    long long bal_tokens;  // > 0: equal lengths; every grp CTAs take this many consecutive tokens of the
+                           // (sequence, q/k head) groups in order, one CTA per value head of the group
+                           // (at most two pieces of units each); nseg = 1
 };
 
 // First token to process for a segment whose outputs start at token a of a
@@ -233,90 +236,127 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
     extern __shared__ float4 smem_f4[];
     __shared__ long long seg_start;
     float* sm = reinterpret_cast<float*>(smem_f4);
-    const int seg = blockIdx.x % p.nseg, unit = blockIdx.x / p.nseg;
-    const int pos = unit / p.h_v, h = unit - pos * p.h_v, hk = h / p.grp;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = warp * 16, c0 = lane * 4;
-    int n = 0;
-    long long s0 = 0, s1 = 0;
-    if (!seq_of(p.order, pos, p.num_seqs, n)) return;
-    if (!seq_bounds(p.cu, n, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
-    // this CTA stores the outputs of tokens [seg_a, t1)
-    const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + BLK - 1) / BLK * BLK;
-    const long long seg_a = s0 + seg * seg_len;
-    if (seg > 0 && seg_a >= s1) return;  // an empty segment
-    const long long t1 = seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1;
-    if (warp == 0) {
-        const long long ts = seg > 0 ? segment_prefix_start<TIn>(p, s0, seg_a, h, hk, lane) : s0;
-        if (lane == 0) seg_start = ts;
-    }
-    __syncthreads();
-    const long long t0 = seg_start;  // first token processed
-    const size_t st_off = ((size_t)n * p.h_v + h) * D * D;
     TOut* o = static_cast<TOut*>(p.o);
+    // this CTA's work: a segment of one (sequence, value head) unit, or with
+    // bal_tokens the end of one unit and the start of the next (pieces): it
+    // stores the outputs of tokens [seg_a, t1) of sequence n, value head h
+    struct Piece { long long seg_a, t1, s0, s1; int n, h; };
+    Piece pc0{}, pc1{};
+    int npieces = 0;
+    if (p.bal_tokens == 0) {
+        const int seg = blockIdx.x % p.nseg, unit = blockIdx.x / p.nseg;
+        const int pos = unit / p.h_v, h = unit - pos * p.h_v;
+        int n = 0;
+        long long s0 = 0, s1 = 0;
+        if (!seq_of(p.order, pos, p.num_seqs, n)) return;
+        if (!seq_bounds(p.cu, n, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+        const long long seg_len = ((s1 - s0 + p.nseg - 1) / p.nseg + BLK - 1) / BLK * BLK;
+        const long long seg_a = s0 + seg * seg_len;
+        if (seg > 0 && seg_a >= s1) return;  // an empty segment
+        pc0 = Piece{seg_a, seg_len > 0 && seg_a + seg_len < s1 ? seg_a + seg_len : s1, s0, s1, n, h};
+        npieces = 1;
+    } else {
+        // tokens of the (sequence, q/k head) groups in order; the grp value
+        // heads of a group take the same share in neighbouring CTAs
+        const long long gtot = (long long)p.num_seqs * p.h_qk * p.eq_len;
+        const int r = blockIdx.x % p.grp;
+        long long a = (long long)(blockIdx.x / p.grp) * p.bal_tokens;
+        const long long b = min(a + p.bal_tokens, gtot);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            if (a >= b) break;
+            const long long u = a / p.eq_len, lo = a - u * p.eq_len, hi = min(p.eq_len, lo + (b - a));
+            const int h = (int)(u % p.h_qk) * p.grp + r, pos = (int)(u / p.h_qk);
+            int n = 0;
+            long long s0 = 0, s1 = 0;
+            if (!seq_of(p.order, pos, p.num_seqs, n)) return;
+            if (!seq_bounds(p.cu, n, p.num_seqs, p.total, p.eq_len, s0, s1)) return;
+            const Piece x{s0 + lo, min(s0 + hi, s1), s0, s1, n, h};
+            if (i == 0) pc0 = x; else pc1 = x;
+            ++npieces;
+            a += hi - lo;
+        }
+        if (npieces == 0) return;
+    }
+    for (int ip = 0; ip < npieces; ++ip) {
+        const Piece pc = pc0;  // the current piece (pc1 moves up at the end)
+        const long long seg_a = pc.seg_a, t1 = pc.t1, s0 = pc.s0, s1 = pc.s1;
+        const int n = pc.n, h = pc.h, hk = h / p.grp;
+        __syncthreads();  // seg_start and the stage of the previous piece are free
+        if (warp == 0) {
+            const long long ts = seg_a > s0 ? segment_prefix_start<TIn>(p, s0, seg_a, h, hk, lane) : s0;
+            if (lane == 0) seg_start = ts;
+        }
+        __syncthreads();
+        const long long t0 = seg_start;  // first token processed
+        const size_t st_off = ((size_t)n * p.h_v + h) * D * D;
 
-    float S[16][4];
-    if (p.h0 && t0 == s0) bwd::load_state(S, p.h0 + st_off, r0, c0);
-    else bwd::zero_state(S);
-    for (long long tb0 = t0; tb0 < t1; tb0 += BLK) {
-        const int nt = (int)min((long long)BLK, t1 - tb0);
-        __syncthreads();
-        kda_stage<TIn>(sm, p, tb0, nt, h, hk);
-        __syncthreads();
-        for (int j = 0; j < nt; ++j) {
-            float ak[16], aq[16];
-#pragma unroll
-            for (int r = 0; r < 16; r += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(sm + OFF_AK + j * D + r0 + r);
-                ak[r] = x.x; ak[r + 1] = x.y; ak[r + 2] = x.z; ak[r + 3] = x.w;
-                const float4 y = *reinterpret_cast<const float4*>(sm + OFF_AQ + j * D + r0 + r);
-                aq[r] = y.x; aq[r + 1] = y.y; aq[r + 2] = y.z; aq[r + 3] = y.w;
-            }
-            float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    ks[c] = fmaf(S[r][c], ak[r], ks[c]);
-                    qs[c] = fmaf(S[r][c], aq[r], qs[c]);
-                }
-            float* red = sm + OFF_RED;
-            *reinterpret_cast<float4*>(red + warp * RED + c0) = make_float4(ks[0], ks[1], ks[2], ks[3]);
-            *reinterpret_cast<float4*>(red + (NW + warp) * RED + c0) = make_float4(qs[0], qs[1], qs[2], qs[3]);
+        float S[16][4];
+        if (p.h0 && t0 == s0) bwd::load_state(S, p.h0 + st_off, r0, c0);
+        else bwd::zero_state(S);
+        for (long long tb0 = t0; tb0 < t1; tb0 += BLK) {
+            const int nt = (int)min((long long)BLK, t1 - tb0);
             __syncthreads();
-            {
-                const int colx = threadIdx.x >> 1, part = threadIdx.x & 1;
-                float sk = 0.f, sq = 0.f;
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    sk += red[(part * 4 + m) * RED + colx];
-                    sq += red[(NW + part * 4 + m) * RED + colx];
-                }
-                sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-                sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-                if (part == 0) {
-                    const float uu = sm[OFF_B + j] * (sm[OFF_V + j * D + colx] - sk);
-                    sm[OFF_U + colx] = uu;
-                    if (tb0 + j >= seg_a)  // the segment's prefix tokens are not stored
-                        o[((size_t)(tb0 + j) * p.h_v + h) * D + colx] = from_f32<TOut>(p.scale * fmaf(sm[OFF_KQ + j], uu, sq));
-                }
-            }
+            kda_stage<TIn>(sm, p, tb0, nt, h, hk);
             __syncthreads();
-            const float4 u4 = *reinterpret_cast<const float4*>(sm + OFF_U + c0);
-            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+            for (int j = 0; j < nt; ++j) {
+                float ak[16], aq[16];
 #pragma unroll
-            for (int r = 0; r < 16; r += 4) {
-                const float4 a4 = *reinterpret_cast<const float4*>(sm + OFF_A + j * D + r0 + r);
-                const float4 k4 = *reinterpret_cast<const float4*>(sm + OFF_K + j * D + r0 + r);
-                const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+                for (int r = 0; r < 16; r += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(sm + OFF_AK + j * D + r0 + r);
+                    ak[r] = x.x; ak[r + 1] = x.y; ak[r + 2] = x.z; ak[r + 3] = x.w;
+                    const float4 y = *reinterpret_cast<const float4*>(sm + OFF_AQ + j * D + r0 + r);
+                    aq[r] = y.x; aq[r + 1] = y.y; aq[r + 2] = y.z; aq[r + 3] = y.w;
+                }
+                float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
+                for (int r = 0; r < 16; ++r)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) S[r + rr][c] = fmaf(av[rr], S[r + rr][c], kv[rr] * u[c]);
+                    for (int c = 0; c < 4; ++c) {
+                        ks[c] = fmaf(S[r][c], ak[r], ks[c]);
+                        qs[c] = fmaf(S[r][c], aq[r], qs[c]);
+                    }
+                float* red = sm + OFF_RED;
+                *reinterpret_cast<float4*>(red + warp * RED + c0) = make_float4(ks[0], ks[1], ks[2], ks[3]);
+                *reinterpret_cast<float4*>(red + (NW + warp) * RED + c0) = make_float4(qs[0], qs[1], qs[2], qs[3]);
+                __syncthreads();
+                {
+                    const int colx = threadIdx.x >> 1, part = threadIdx.x & 1;
+                    float sk = 0.f, sq = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        sk += red[(part * 4 + m) * RED + colx];
+                        sq += red[(NW + part * 4 + m) * RED + colx];
+                    }
+                    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+                    if (part == 0) {
+                        const float uu = sm[OFF_B + j] * (sm[OFF_V + j * D + colx] - sk);
+                        sm[OFF_U + colx] = uu;
+                        if (tb0 + j >= seg_a)  // the piece's prefix tokens are not stored
+                            o[((size_t)(tb0 + j) * p.h_v + h) * D + colx] = from_f32<TOut>(p.scale * fmaf(sm[OFF_KQ + j], uu, sq));
+                    }
+                }
+                __syncthreads();
+                const float4 u4 = *reinterpret_cast<const float4*>(sm + OFF_U + c0);
+                const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                for (int r = 0; r < 16; r += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(sm + OFF_A + j * D + r0 + r);
+                    const float4 k4 = *reinterpret_cast<const float4*>(sm + OFF_K + j * D + r0 + r);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) S[r + rr][c] = fmaf(av[rr], S[r + rr][c], kv[rr] * u[c]);
+                }
             }
         }
+        if (p.hT && t1 == s1) bwd::store_state(S, p.hT + st_off, r0, c0);  // the piece ends its sequence
+        pc0 = pc1;
     }
-    if (p.hT && t1 == s1) bwd::store_state(S, p.hT + st_off, r0, c0);  // the last segment
 }
 
 }  // namespace kda

@@ -291,16 +291,31 @@ namespace {
 template <typename TIn, typename TOut>
 gdn_status launch_kda_prefill(gdn::kda::Args a, cudaStream_t s) {
     const DevInfo di = dev_info();
-    // fewer units than two per SM: sequence segments (not when the final
-    // state overwrites the initial state: a later segment could then finish
-    // before an earlier one has read it)
+    // fewer units than two per SM: split the units over several CTAs (not
+    // when the final state overwrites the initial state: a later piece could
+    // then finish before an earlier one has read it). Equal lengths: shares
+    // of at least 256 tokens of the (sequence, q/k head) groups in order,
+    // each taken by the group's value heads in neighbouring CTAs, so that
+    // every slot gets the same work; otherwise sequence segments of at least
+    // 512 tokens.
     a.nseg = 1;
+    a.bal_tokens = 0;
     const long long units = (long long)a.num_seqs * a.h_v, slots = 2LL * std::max(di.sms, 1);
+    long long blocks = units;
     if (units > 0 && units < slots && !(a.hT != nullptr && a.hT == a.h0)) {
-        const long long by_len = (long long)(a.total / a.num_seqs) / 512;
-        a.nseg = (int)std::max(1LL, std::min(std::min(slots / units, by_len), 64LL));
+        const long long gtot = (long long)a.num_seqs * a.h_qk * a.eq_len;  // eq_len = 0 with cu_seqlens
+        const long long share_slots = std::max(1LL, slots / a.grp);
+        const long long share = (gtot + share_slots - 1) / share_slots / gdn::kda::BLK * gdn::kda::BLK +
+                                gdn::kda::BLK;  // rounded up to whole blocks
+        if (a.cu == nullptr && a.eq_len > 0 && share >= 256 && share < a.eq_len) {
+            a.bal_tokens = share;
+            blocks = (gtot + share - 1) / share * a.grp;
+        } else {
+            const long long by_len = (long long)(a.total / a.num_seqs) / 512;
+            a.nseg = (int)std::max(1LL, std::min(std::min(slots / units, by_len), 64LL));
+            blocks = units * a.nseg;
+        }
     }
-    const long long blocks = units * a.nseg;
     if (blocks > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED;
     if (di.smem_optin < (int)gdn::kda::SMEM_BYTES) return di.smem_optin <= 0 ? GDN_ERR_CUDA : GDN_ERR_UNSUPPORTED;
     auto kern = gdn::kda::kda_prefill_kernel<TIn, TOut>;

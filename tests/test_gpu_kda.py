@@ -61,6 +61,22 @@ def test_prefill_sequence_segments():
     assert_parity(S, S_ref, TAU_F32, "final state")
 
 
+def test_prefill_balanced_shares():
+    """An equal-length batch with few units: the prefill cuts the tokens of the
+    (sequence, q/k head) groups into balanced shares (here 288 tokens), each
+    taken by the group's two value heads in neighbouring CTAs; most CTAs
+    finish one unit and start the next. Every output and final state against
+    the oracle, at the fp32 bound."""
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16", batch=1, seqlen=20000,
+                                h0_std=0.02, seed=45)
+    assert d["cu_seqlens"] is None
+    g = gdn_inputs.make_channel_decay((20000, 4, 128), seed=45)
+    o, S = _kda_gpu(d, g)
+    o_ref, S_ref = oracle.kda_recurrent(d["q"], d["k"], d["v"], g, d["beta"], h0=d["h0"], cu_seqlens=_cu(d))
+    assert_parity(o, o_ref, TAU_F32, "o")
+    assert_parity(S, S_ref, TAU_F32, "final state")
+
+
 def test_prefill_fp32_equal_length_bf16_output_and_order():
     d = gdn_inputs.make_prefill(h_qk=2, h_v=2, d_k=128, d_v=128, dtype="f32", batch=3, seqlen=45, seed=42)
     g = gdn_inputs.make_channel_decay((135, 2, 128), g_shift=-3.0, seed=42)
