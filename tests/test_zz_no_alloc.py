@@ -5,11 +5,12 @@ same backward kernel as gdn_chunk_bwd on a 64 MiB scratch array built into
 the library instead of a caller workspace.
 
 The test calls it through the C ABI twice in a row, on two different
-problems, and compares each result with gdn_chunk_bwd's (caller workspace)
-under the gradient tolerance of the backward parity tests. The second call
-runs on whatever the first left in the shared array. It also checks that a
-problem larger than the array is refused before anything runs. The file is
-named so that pytest collects it last.
+problems, and compares each result with the fp64 gradient oracle and with
+gdn_chunk_bwd's (caller workspace), under the gradient tolerance of the
+backward parity tests. The second call runs on whatever the first left in
+the shared array. It also checks that a problem larger than the array is
+refused before anything runs. The file is named so that pytest collects it
+last.
 """
 import ctypes
 
@@ -18,6 +19,7 @@ import pytest
 import torch
 
 import gdn_inputs
+import oracle
 import gated_deltanet_recurrence_05_b300 as gdn
 from gdn_testutil import assert_parity
 
@@ -33,7 +35,9 @@ def _problem(seed, lengths, h_qk, h_v):
                                 h0_std=0.02, seed=seed)
     gr = gdn_inputs.make_grads(d, dtype="bf16", dht_std=0.05, seed=seed)
     dd = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
-    return dd, gr["do"].cuda(), gr["dht"].cuda()
+    ref = oracle.recurrent_backward(d["q"], d["k"], d["v"], d["g"], d["beta"], gr["do"], h0=d["h0"],
+                                    dht=gr["dht"], cu_seqlens=d["cu_seqlens"])
+    return dd, gr["do"].cuda(), gr["dht"].cuda(), ref
 
 
 def _static(dd, do, dht):
@@ -63,13 +67,14 @@ def _with_workspace(dd, do, dht):
 
 def test_static_scratch_two_calls_match_workspace_entry_point():
     problems = [_problem(31, [70, 33, 1], 2, 4), _problem(32, [129, 0, 64], 4, 4)]
-    for i, (dd, do, dht) in enumerate(problems):
+    for i, (dd, do, dht, oref) in enumerate(problems):
         need = gdn.chunk_bwd_workspace_size(dd["cu_seqlens"].numel() - 1, dd["q"].shape[0],
                                             dd["q"].shape[1], dd["v"].shape[1])
         assert 0 < need <= SCRATCH_BYTES
         got = _static(dd, do, dht)
         ref = _with_workspace(dd, do, dht)
         for name, x, y in zip(("dq", "dk", "dv", "dg", "dbeta", "dh0"), got, ref):
+            assert_parity(x, oref[name], TAU_BWD, f"call {i + 1}: {name} vs oracle")
             assert_parity(x, y, TAU_BWD, f"call {i + 1}: {name}")
 
 
