@@ -45,3 +45,28 @@ def test_wait_timeout_unwinds_reports_and_leaves_stream_usable():
     assert_parity(o.cpu().numpy(), o_ref, TAU_BF16, "o after the timed-out call")
     assert_parity(S.cpu().numpy(), S_ref, TAU_BF16, "final state after the timed-out call")
 
+
+
+def test_wait_timeout_with_balanced_shares():
+    """The same failure path when every CTA holds two pieces of units (an
+    equal-length batch cut into balanced shares): the withheld arrival is the
+    CTA's second chunk; every CTA gives up, unwinds and leaves the stream
+    usable for an exact ordinary call."""
+    d = gdn_inputs.make_prefill(h_qk=2, h_v=4, d_k=128, d_v=128, dtype="bf16", batch=2, seqlen=640,
+                                h0_std=0.02, seed=42)
+    dd = to_cuda(d)
+    stream = torch.cuda.current_stream()
+    assert gdn.get_device_error() == 0
+    gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], None, num_seqs=2,
+                  output_dtype=torch.float32, test_wait_timeout=True, balance=True, stream=stream)
+    code = ctypes.c_uint32(0)
+    st = gdn.lib().gdn_get_device_error(ctypes.c_void_p(stream.cuda_stream), ctypes.byref(code))
+    assert st == 4, gdn.lib().gdn_status_string(st)
+    assert code.value & gdn.DEVERR_TIMEOUT
+    o, S = gdn.chunk_fwd(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["h0"], None, num_seqs=2,
+                         output_dtype=torch.float32, balance=True, stream=stream)
+    assert gdn.get_device_error() == 0
+    o_ref, S_ref = oracle.recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"], h0=d["h0"],
+                                    cu_seqlens=torch.tensor([0, 640, 1280], dtype=torch.int32))
+    assert_parity(o.cpu().numpy(), o_ref, TAU_BF16, "o after the timed-out call")
+    assert_parity(S.cpu().numpy(), S_ref, TAU_BF16, "final state after the timed-out call")
