@@ -802,9 +802,10 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant_
             const float* gb = gb_slot(n);
             const uint32_t ph = (uint32_t)(n >> 1) & 1u;  // phase parity of the per-parity barriers
             bool ok = WAITW(B_GB_FULL + n % GB_SLOTS, (n / GB_SLOTS) & 1) && WAITW(B_XREADY0 + g, ph);
-            // P and Bw/Bu buffers g were last read by the products of chunk n - 2
-            if (ok && wq >= 2 && n >= 2) ok = WAITW(B_PFREE0 + g, ph ^ 1u);
-            if (ok && n >= 2) ok = WAITW(B_M2W0 + g, ph ^ 1u) && WAITW(B_M2U0 + g, ph ^ 1u);
+            // P and Bw/Bu buffers g were last read by the products of chunk n - 2:
+            // M2w(n - 2) was issued before M1(n) by the same thread (XREADY(n)
+            // completes after it), M2u(n - 2) before M4(n - 2) (PFREE)
+            if (ok && n >= 2) ok = WAITW(B_PFREE0 + g, ph ^ 1u);
             if (named_sync_or(bar_id, 128, !ok)) break;
             if (gt == 0) GDN_TRACE_AT(0, n);
             tc_fence_after();
