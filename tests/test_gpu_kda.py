@@ -86,6 +86,26 @@ def test_prefill_fp32_equal_length_bf16_output_and_order():
     assert_parity(S, S_ref, TAU_F32, "final state")
 
 
+def test_prefill_strong_and_zero_decay_chunks():
+    """Extreme per-channel decays: strong decays (g ~ -8 per token, so the
+    state forgets within a few tokens and products of decays underflow), a
+    weak stretch inside the same sequence, no decay at all (g = 0, alpha = 1),
+    and half the channels strong with the other half weak in one sequence;
+    every output and final state against the oracle at the fp32 bound."""
+    d = gdn_inputs.make_prefill(h_qk=1, h_v=2, d_k=128, d_v=128, dtype="bf16", lengths=[200, 150, 70],
+                                h0_std=0.02, seed=46)
+    T = sum(d["lengths"])
+    g = gdn_inputs.make_channel_decay((T, 2, 128), g_shift=8.0, seed=46)
+    weak = gdn_inputs.make_channel_decay((T, 2, 128), g_shift=-3.0, seed=47)
+    g[90:160] = weak[90:160]           # sequence 0: strong, weak, strong
+    g[200:350] = 0.0                   # sequence 1: no decay
+    g[350:, :, 64:] = weak[350:, :, 64:]  # sequence 2: channels 0-63 strong, 64-127 weak
+    o, S = _kda_gpu(d, g)
+    o_ref, S_ref = oracle.kda_recurrent(d["q"], d["k"], d["v"], g, d["beta"], h0=d["h0"], cu_seqlens=_cu(d))
+    assert_parity(o, o_ref, TAU_F32, "o")
+    assert_parity(S, S_ref, TAU_F32, "final state")
+
+
 def test_uniform_channels_equal_gated_delta_rule():
     """Equal decays in every channel: KDA must reproduce the gated delta rule
     (the fp32 CUDA-core prefill of gdn_chunk_fwd)."""
