@@ -599,13 +599,53 @@ def run_decode(args, dev, peaks, world):
     us = max_over_ranks(ms * 1e3, world, dev)
     b = decode_algorithmic(wl.num_seqs, wl.h_qk, wl.h_v, wl.d_k, wl.d_v)
     gbs = b / (us / 1e6) / 1e9
+    graph = decode_graph(gdn, dd, state, o, steps, b, peaks, dev, world)
     return {"workload": f"decode: {wl.num_seqs} sequences x H_v={wl.h_v} (H_qk={wl.h_qk}) x 128x128 fp32 "
                         f"states (512 MiB, > L2), bf16 token inputs and output, {steps} in-place steps",
             "us_per_step": us, "steps_per_s": 1e6 / us, "tokens_per_s": wl.num_seqs * 1e6 / us * world,
             "GB_per_s": gbs * world, "gpu_launches": steps, "clocks": clk.summary(),
-            "timing": _timing(per, ms, 1e3, "us per step"), "cold_first_call": cold,
+            "timing": _timing(per, ms, 1e3, "us per step"), "cold_first_call": cold, "graph": graph,
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": int(b)}}
+
+
+def decode_graph(gdn, dd, state, o, steps, b, peaks, dev, world):
+    """The same `steps` consecutive decode steps (each its own pregenerated
+    token) captured once through the C ABI into a CUDA Graph and replayed as
+    one launch; timed with CUDA events around a replay after one untimed
+    replay. Returns the per-step time, or the capture's error message."""
+    try:
+        cg = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.graph(cg, stream=side):
+            cap = torch.cuda.current_stream(dev)
+            for t in range(steps):
+                gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state,
+                                out=o, stream=cap)
+    except Exception as e:  # a capture the runtime refused: report it, keep the run
+        torch.cuda.synchronize(dev)
+        return {"error": f"{type(e).__name__}: {e}"[:300]}
+    stream = torch.cuda.current_stream(dev)
+    state.copy_(dd["state"])
+    cg.replay()                      # untimed
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    cg.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    if gdn.get_device_error() != 0:
+        raise RuntimeError("device error in the decode graph")
+    us = max_over_ranks(e0.elapsed_time(e1) * 1e3 / steps, world, dev)
+    gbs = b / (us / 1e6) / 1e9
+    del cg
+    return {"steps": steps, "gpu_launches": steps, "us_per_step": us, "GB_per_s": gbs * world,
+            "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "how": f"{steps} decode steps captured into one CUDA Graph through the C ABI, replayed once untimed "
+                   f"and once timed (CUDA events around the replay)"}
 
 
 def run_epilogue(args, dev, peaks, world, o_shape):

@@ -95,3 +95,32 @@ def test_decode_matches_prefill():
         torch.cuda.synchronize()
         assert_parity(o_dec[:, n], o_pf.cpu().numpy(), TAU_F32, "o decode vs prefill")
         assert_parity(S_dec[n], S_pf[0].cpu().numpy(), TAU_F32, "state decode vs prefill")
+
+
+def test_decode_steps_captured_in_a_cuda_graph():
+    """Consecutive decode steps issued through the C ABI inside a CUDA Graph
+    capture (the way a serving loop replays them) and replayed: outputs and
+    state against the oracle, and the replay equals the same steps run
+    eagerly, bit for bit."""
+    d = gdn_inputs.make_decode(num_seqs=6, h_qk=2, h_v=4, d_k=128, d_v=128, steps=8, seed=9)
+    dd = to_cuda(d)
+    state = dd["state"].clone()
+    outs = torch.empty(8, 6, 4, 128, dtype=torch.float32, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        cap = torch.cuda.current_stream()
+        for t in range(8):
+            gdn.decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t], state,
+                            out=outs[t], stream=cap)
+    state.copy_(dd["state"])  # the capture ran nothing; start from the initial states
+    graph.replay()
+    torch.cuda.synchronize()
+    assert gdn.get_device_error() == 0
+    o_ref, S_ref = oracle.decode_steps(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"])
+    assert_parity(outs.cpu().numpy(), o_ref, TAU_BF16, "o (graph)")
+    assert_parity(state.cpu().numpy(), S_ref, TAU_BF16, "state (graph)")
+    o_eager, S_eager = _run_steps(d, 8, torch.float32)
+    assert np.array_equal(outs.cpu().numpy(), o_eager)
+    assert np.array_equal(state.cpu().numpy(), S_eager)
