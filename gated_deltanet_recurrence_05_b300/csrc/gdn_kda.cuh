@@ -21,10 +21,9 @@ namespace gdn {
 namespace kda {
 
 constexpr int D = 128;
-constexpr int BLK = 32;        // tokens staged per block
+constexpr int BLK = 32;        // granularity of prefill segments and shares (tokens)
 constexpr int NT = 256;
 constexpr int NW = NT / 32;
-constexpr int RED = 132;
 
 // Decode step: one CTA of 8 warps per (n, h), the layout of decode_d128_kernel
 // (warp w owns columns 16w..16w+15; lane l holds 4 columns of rows
@@ -111,22 +110,90 @@ kda_decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, con
     }
 }
 
-// Prefill: one CTA of 256 threads per (sequence, value head) walks the
-// sequence token by token with the state in registers (thread: rows
-// 16w..16w+15, columns 4l..4l+3); blocks of 32 tokens are staged in shared
-// memory with a o k, a o q, a and k . q precomputed. Two block barriers per
-// token (one column-sum exchange for both reads, one to publish u).
-constexpr int OFF_K = 0;
-constexpr int OFF_AK = OFF_K + BLK * D;
-constexpr int OFF_AQ = OFF_AK + BLK * D;
-constexpr int OFF_A = OFF_AQ + BLK * D;
-constexpr int OFF_V = OFF_A + BLK * D;
-constexpr int OFF_U = OFF_V + BLK * D;
-constexpr int OFF_RED = OFF_U + D;
-constexpr int OFF_B = OFF_RED + 2 * NW * RED;
-constexpr int OFF_KQ = OFF_B + BLK;
-constexpr int SMEM_FLOATS = OFF_KQ + BLK;
+// Prefill: chunks of C = 16 tokens in the WY form of the rule. Within a
+// chunk, with G_t = sum_{u <= t} g_u per key channel (from the chunk start)
+// and S0 the state before the chunk, the unrolled rule gives S~_t =
+// diag(exp(G_t)) S0 + sum_{s<t} diag(exp(G_t - G_s)) beta_s k_s e_s^T, so the
+// errors e_t, outputs and next state are
+//
+//   A_ts = beta_s sum_i k_si k_ti exp(G_ti - G_si)   (s < t)
+//   P_ts = beta_s sum_i k_si q_ti exp(G_ti - G_si)   (s <= t)
+//   E    = (I + A)^{-1} (V - K_G S0),   K_G = rows k_t o exp(G_t)
+//   O    = scale (Q_G S0 + P E),        Q_G = rows q_t o exp(G_t)
+//   S_L  = diag(exp(G_L)) S0 + K_T^T diag(beta) E,  K_T = rows k_t o exp(G_L - G_t)
+//
+// Every decay factor is the exponential of a difference G_t - G_s <= 0 (or
+// G_t <= 0), so none exceeds 1. A and P fold the factor into rows scaled by
+// exp(G_t) and exp(-G_s) while every running sum of the chunk is within
+// 2^+-100, and take it per element otherwise.
+//
+// One CTA of 256 threads per piece; warp w owns state columns 16w..16w+15
+// and keeps S^T (16 columns x 128 rows) in fp32 registers as the accumulator
+// fragments of the warp MMA (m16n8k8, tf32): lane (g, c) = (lane / 4,
+// lane % 4) holds rows 8j + 2c, 8j + 2c + 1 of columns 16w + g, 16w + g + 8,
+// j = 0..15. The three state products of a chunk, S0^T K_G^T, S0^T Q_G^T and
+// U^T K_T (U = diag(beta) E), run on the tensor cores with fp32 accuracy:
+// each fp32 operand x is split into tf32 parts x = hi + lo and the product
+// taken as hi hi + hi lo + lo hi (fp32 accumulation). The contraction index
+// of each 8-wide step is taken in the order (2c, 2c + 1 for c = 0..3) on both
+// operands, which makes the state's accumulator fragments its A fragments
+// without any data movement. The triangular solve and the outputs run per
+// column on lanes 0-15 of each warp; the chunk's tiles (k, q, v, the decays,
+// A and P) are shared through shared memory.
+constexpr int C = 16;                  // tokens per chunk
+constexpr int XS = D + 8;              // row stride of K_G, Q_G, K_I ([token][channel]): conflict-free fragments
+constexpr int KS = C + 8;              // row stride of K_T^T ([channel][token])
+// |running log2-decay| up to which exp(-G) and exp(G) stay normal fp32
+// numbers (2^100 and 2^-100) and their product keeps full precision
+constexpr float G2_MAX = 100.f;
+constexpr int OFF_K = 0;               // k   [C][D]
+constexpr int OFF_Q = OFF_K + C * D;   // q   [C][D]
+constexpr int OFF_V = OFF_Q + C * D;   // v   [C][D]
+constexpr int OFF_G2 = OFF_V + C * D;  // g as loaded, then G / ln 2 [C][D] (running sums, base 2)
+constexpr int OFF_KG = OFF_G2 + C * D; // K_G [C][XS]
+constexpr int OFF_QG = OFF_KG + C * XS;
+constexpr int OFF_KI = OFF_QG + C * XS;  // K_I = rows k_t o exp(-G_t) [C][XS]
+constexpr int OFF_KTT = OFF_KI + C * XS; // K_T^T [D][KS]
+constexpr int OFF_GL = OFF_KTT + D * KS; // exp(G_L) [D]
+constexpr int OFF_AM = OFF_GL + D;       // A [C][C]
+constexpr int OFF_PM = OFF_AM + C * C;   // P [C][C]
+constexpr int OFF_BT = OFF_PM + C * C;   // beta [C]
+constexpr int OFF_WS = OFF_BT + C;       // per warp: S0^T K_G, S0^T Q_G [2][C][16], then beta E [C][16]
+constexpr int WS_FLOATS = 3 * C * 16;
+constexpr int SMEM_FLOATS = OFF_WS + NW * WS_FLOATS;
 constexpr size_t SMEM_BYTES = (size_t)SMEM_FLOATS * sizeof(float);
+static_assert(OFF_KG % 4 == 0 && OFF_KTT % 4 == 0 && OFF_WS % 4 == 0 && XS % 4 == 0 && KS % 2 == 0,
+              "vector alignment");
+static_assert(2 * SMEM_BYTES + 2048 <= 232448, "two CTAs per SM");
+
+__device__ __forceinline__ float ex2f(float x) {  // 2^x on the special-function unit
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// x = hi + lo with hi, lo tf32 (round to nearest): hi holds the top 11 bits
+// of the significand and lo the next 11, so hi hi + hi lo + lo hi carries
+// about 22 bits of each product
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float r = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+// D += A B on the warp MMA, m16n8k8, tf32 operands, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A B to about fp32 accuracy from split operands (small terms first)
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                     const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    mma_tf32(d, al, bh[0], bh[1]);
+    mma_tf32(d, ah, bl[0], bl[1]);
+    mma_tf32(d, ah, bh[0], bh[1]);
+}
 
 struct Args {
     const void* q; const void* k; const void* v;
@@ -185,14 +252,20 @@ __device__ __forceinline__ long long segment_prefix_start(const Args& p, long lo
     return s0;
 }
 
+// Stage tokens [tb0, tb0 + n) of the piece into shared memory as fp32 (rows
+// j >= n: k = q = v = 0, g = 0, beta = 0, which leave the state unchanged),
+// then the running sums of g (one thread per channel, in place) and the
+// chunk's decayed rows (thread (half hf, channel i): the tokens of its half).
+// Returns whether some running sum is beyond +-G2_MAX (a block-wide OR).
 template <typename TIn>
-__device__ __forceinline__ void kda_stage(float* sm, const Args& p, long long tb0, int n, int h, int hk) {
+__device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long long tb0, int n, int h, int hk) {
+    constexpr float LOG2E = 1.4426950408889634f;
     const TIn* q = static_cast<const TIn*>(p.q);
     const TIn* k = static_cast<const TIn*>(p.k);
     const TIn* v = static_cast<const TIn*>(p.v);
-    for (int idx = threadIdx.x; idx < BLK * (D / 4); idx += NT) {
+    for (int idx = threadIdx.x; idx < C * (D / 4); idx += NT) {
         const int j = idx >> 5, c = (idx & 31) * 4;
-        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk, vv = kk, aa = make_float4(1.f, 1.f, 1.f, 1.f);
+        float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk, vv = kk, gg = kk;
         if (j < n) {
             const long long t = tb0 + j;
             const size_t qk_off = ((size_t)t * p.h_qk + hk) * D + c;
@@ -200,44 +273,141 @@ __device__ __forceinline__ void kda_stage(float* sm, const Args& p, long long tb
             kk = load4(k + qk_off);
             qq = load4(q + qk_off);
             vv = load4(v + v_off);
-            const float4 gg = *reinterpret_cast<const float4*>(p.g + v_off);
-            aa = make_float4(expf(gg.x), expf(gg.y), expf(gg.z), expf(gg.w));
+            gg = *reinterpret_cast<const float4*>(p.g + v_off);
         }
         *reinterpret_cast<float4*>(sm + OFF_K + j * D + c) = kk;
-        *reinterpret_cast<float4*>(sm + OFF_AK + j * D + c) =
-            make_float4(aa.x * kk.x, aa.y * kk.y, aa.z * kk.z, aa.w * kk.w);
-        *reinterpret_cast<float4*>(sm + OFF_AQ + j * D + c) =
-            make_float4(aa.x * qq.x, aa.y * qq.y, aa.z * qq.z, aa.w * qq.w);
-        *reinterpret_cast<float4*>(sm + OFF_A + j * D + c) = aa;
+        *reinterpret_cast<float4*>(sm + OFF_Q + j * D + c) = qq;
         *reinterpret_cast<float4*>(sm + OFF_V + j * D + c) = vv;
+        *reinterpret_cast<float4*>(sm + OFF_G2 + j * D + c) = gg;
     }
-    // k . q per token: warp w takes tokens w, w + 8, ... (lanes: 4 channels each)
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int j = warp; j < BLK; j += NW) {
-        float x = 0.f;
-        if (j < n) {
-            const size_t qk_off = ((size_t)(tb0 + j) * p.h_qk + hk) * D + 4 * lane;
-            const float4 kk = load4(k + qk_off), qq = load4(q + qk_off);
-            x = kk.x * qq.x + kk.y * qq.y + kk.z * qq.z + kk.w * qq.w;
+    if (threadIdx.x < C) sm[OFF_BT + threadIdx.x] = threadIdx.x < n ? p.beta[(size_t)(tb0 + threadIdx.x) * p.h_v + h] : 0.f;
+    __syncthreads();
+    const int hf = threadIdx.x >> 7, i = threadIdx.x & (D - 1);
+    if (hf == 0) {  // running sums of g, in place, one thread per channel
+        float gv[C];
+#pragma unroll
+        for (int j = 0; j < C; ++j) gv[j] = sm[OFF_G2 + j * D + i];
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            acc = fmaf(gv[j], LOG2E, acc);
+            sm[OFF_G2 + j * D + i] = acc;
         }
-        x = warp_sum(x);
-        if (lane == 0) sm[OFF_KQ + j] = x;
+        sm[OFF_GL + i] = ex2f(acc);
     }
-    if (threadIdx.x < BLK) sm[OFF_B + threadIdx.x] = threadIdx.x < n ? p.beta[(size_t)(tb0 + threadIdx.x) * p.h_v + h] : 0.f;
+    __syncthreads();
+    const float acc = sm[OFF_G2 + (C - 1) * D + i];
+    bool wide = false;  // a running sum outside [-G2_MAX, G2_MAX]: exp(-G) could overflow
+#pragma unroll
+    for (int jj = 0; jj < C / 2; ++jj) {
+        const int j = (C / 2) * hf + jj;
+        const float gm = sm[OFF_G2 + j * D + i];
+        const float e = ex2f(gm), kj = sm[OFF_K + j * D + i];
+        wide |= fabsf(gm) > G2_MAX;
+        sm[OFF_KG + j * XS + i] = kj * e;
+        sm[OFF_QG + j * XS + i] = sm[OFF_Q + j * D + i] * e;
+        sm[OFF_KTT + i * KS + j] = kj * ex2f(acc - gm);
+        sm[OFF_KI + j * XS + i] = kj * ex2f(-gm);
+    }
+    return __syncthreads_or(wide) != 0;
 }
 
-// Two CTAs fit on an SM (at most 128 registers per thread, 91 KB of shared
+// A and P of the staged chunk on the warp MMA when the decay factors fold
+// into the rows (no running sum beyond +-G2_MAX): warps 0-3 take one 16 x 8
+// block each (A or P; the columns s = 0-7 or 8-15) of K_G K_I^T or Q_G K_I^T
+// over the 128 channels, in fp32 accuracy (split tf32 operands), and store it
+// scaled by beta_s. Entries outside s < t (A) or s <= t (P) are stored too and
+// never read.
+__device__ __forceinline__ void kda_chunk_ap_mma(float* sm, int warp, int lane) {
+    const int fg = lane >> 2, fc = lane & 3;
+    const int isP = warp >> 1, nb = warp & 1;
+    const float* X = sm + (isP ? OFF_QG : OFF_KG);
+    const float* Ki = sm + OFF_KI + (8 * nb + fg) * XS;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int kt = 0; kt < D / 8; ++kt) {
+        const float2 x0 = *reinterpret_cast<const float2*>(X + fg * XS + 8 * kt + 2 * fc);
+        const float2 x1 = *reinterpret_cast<const float2*>(X + (fg + 8) * XS + 8 * kt + 2 * fc);
+        const float2 bv = *reinterpret_cast<const float2*>(Ki + 8 * kt + 2 * fc);
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(x0.x, ah[0], al[0]);
+        split_tf32(x1.x, ah[1], al[1]);
+        split_tf32(x0.y, ah[2], al[2]);
+        split_tf32(x1.y, ah[3], al[3]);
+        split_tf32(bv.x, bh[0], bl[0]);
+        split_tf32(bv.y, bh[1], bl[1]);
+        mma3(d, ah, al, bh, bl);
+    }
+    float* M = sm + (isP ? OFF_PM : OFF_AM);
+    const int s0 = 8 * nb + 2 * fc;
+    const float b0 = sm[OFF_BT + s0], b1 = sm[OFF_BT + s0 + 1];
+    M[fg * C + s0] = b0 * d[0];
+    M[fg * C + s0 + 1] = b1 * d[1];
+    M[(fg + 8) * C + s0] = b0 * d[2];
+    M[(fg + 8) * C + s0 + 1] = b1 * d[3];
+}
+
+// A (thread tid < 120) or P (the other 136) entry of the staged chunk: one
+// dot product over the 128 channels, the channels rotated by lane so that the
+// lanes' 16-byte reads spread over all banks. The decay factor
+// exp(G_t - G_s) = exp(G_t) exp(-G_s) is folded into the rows K_G, Q_G and
+// K_I, unless some running sum of the chunk is beyond +-G2_MAX (base 2), where
+// exp(-G) could overflow: then each factor is taken per element.
+__device__ __forceinline__ void kda_chunk_ap(float* sm, int lane, bool wide) {
+    const bool isA = threadIdx.x < (C * (C - 1)) / 2;
+    int jj = isA ? (int)threadIdx.x : (int)threadIdx.x - (C * (C - 1)) / 2, t = 0;
+    while (jj >= (isA ? t : t + 1)) {  // entries of row t: s < t (A) or s <= t (P)
+        jj -= isA ? t : t + 1;
+        ++t;
+    }
+    const int s = jj;
+    float acc = 0.f;
+    if (!wide) {
+        const float* X = sm + (isA ? OFF_KG : OFF_QG) + t * XS;
+        const float* Ks = sm + OFF_KI + s * XS;
+        float acc2 = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < D / 4; ++m) {
+            const int i = ((m + lane) & (D / 4 - 1)) * 4;
+            const float4 x = *reinterpret_cast<const float4*>(X + i), kk = *reinterpret_cast<const float4*>(Ks + i);
+            acc = fmaf(x.x, kk.x, acc);
+            acc2 = fmaf(x.y, kk.y, acc2);
+            acc = fmaf(x.z, kk.z, acc);
+            acc2 = fmaf(x.w, kk.w, acc2);
+        }
+        acc += acc2;
+    } else {
+        const float* X = sm + (isA ? OFF_K : OFF_Q) + t * D;
+        const float* Ks = sm + OFF_K + s * D;
+        const float* Gt = sm + OFF_G2 + t * D;
+        const float* Gs = sm + OFF_G2 + s * D;
+#pragma unroll 4
+        for (int m = 0; m < D / 4; ++m) {
+            const int i = ((m + lane) & (D / 4 - 1)) * 4;
+            const float4 x = *reinterpret_cast<const float4*>(X + i), kk = *reinterpret_cast<const float4*>(Ks + i);
+            const float4 gt = *reinterpret_cast<const float4*>(Gt + i), gs = *reinterpret_cast<const float4*>(Gs + i);
+            acc = fmaf(x.x * kk.x, ex2f(gt.x - gs.x), acc);
+            acc = fmaf(x.y * kk.y, ex2f(gt.y - gs.y), acc);
+            acc = fmaf(x.z * kk.z, ex2f(gt.z - gs.z), acc);
+            acc = fmaf(x.w * kk.w, ex2f(gt.w - gs.w), acc);
+        }
+    }
+    sm[(isA ? OFF_AM : OFF_PM) + t * C + s] = sm[OFF_BT + s] * acc;
+}
+
+// Two CTAs fit on an SM (at most 128 registers per thread, 99 KB of shared
 // memory): when the (sequence, value head) units are fewer than twice the
 // SMs, each sequence is split into segments (one CTA each), started a few
 // tokens early from a zero state where the decay allows it
-// (segment_prefix_start), so that more warps share each SM.
+// (segment_prefix_start), or, for equal lengths, into balanced shares, so
+// that more warps share each SM.
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
     extern __shared__ float4 smem_f4[];
     __shared__ long long seg_start;
     float* sm = reinterpret_cast<float*>(smem_f4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = warp * 16, c0 = lane * 4;
+    const int fg = lane >> 2, fc = lane & 3;  // fragment row group and column pair
     TOut* o = static_cast<TOut*>(p.o);
     // this CTA's work: a segment of one (sequence, value head) unit, or with
     // bal_tokens the end of one unit and the start of the next (pieces): it
@@ -293,68 +463,129 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
         const long long t0 = seg_start;  // first token processed
         const size_t st_off = ((size_t)n * p.h_v + h) * D * D;
 
-        float S[16][4];
-        if (p.h0 && t0 == s0) bwd::load_state(S, p.h0 + st_off, r0, c0);
-        else bwd::zero_state(S);
-        for (long long tb0 = t0; tb0 < t1; tb0 += BLK) {
-            const int nt = (int)min((long long)BLK, t1 - tb0);
-            __syncthreads();
-            kda_stage<TIn>(sm, p, tb0, nt, h, hk);
-            __syncthreads();
-            for (int j = 0; j < nt; ++j) {
-                float ak[16], aq[16];
+        // S^T fragments: Sd[j] = S[8j + 2c][cg], S[8j + 2c + 1][cg], S[8j + 2c][cg + 8],
+        // S[8j + 2c + 1][cg + 8] with cg = 16 warp + g (lane = 4 g + c)
+        float Sd[D / 8][4];
+        {
+            const float* src = p.h0 + st_off;
+            const bool from_h0 = p.h0 && t0 == s0;
 #pragma unroll
-                for (int r = 0; r < 16; r += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(sm + OFF_AK + j * D + r0 + r);
-                    ak[r] = x.x; ak[r + 1] = x.y; ak[r + 2] = x.z; ak[r + 3] = x.w;
-                    const float4 y = *reinterpret_cast<const float4*>(sm + OFF_AQ + j * D + r0 + r);
-                    aq[r] = y.x; aq[r + 1] = y.y; aq[r + 2] = y.z; aq[r + 3] = y.w;
+            for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    Sd[j][e] = from_h0 ? src[(size_t)(8 * j + 2 * fc + (e & 1)) * D + 16 * warp + fg + 8 * (e >> 1)]
+                                       : 0.f;
+        }
+        float* ws = sm + OFF_WS + warp * WS_FLOATS;
+        for (long long tb0 = t0; tb0 < t1; tb0 += C) {
+            const int nt = (int)min((long long)C, t1 - tb0);
+            __syncthreads();  // the previous chunk's tiles are free
+            const bool wide = kda_stage_chunk<TIn>(sm, p, tb0, nt, h, hk);  // ends with a block barrier
+            if (wide) kda_chunk_ap(sm, lane, true);
+            else if (warp < 4) kda_chunk_ap_mma(sm, warp, lane);
+            // S0^T K_G^T and S0^T Q_G^T (16 columns x 16 tokens each) on the warp MMA
+            {
+                float Y[2][2][4];
+#pragma unroll
+                for (int x = 0; x < 2; ++x)
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) Y[x][n][e] = 0.f;
+#pragma unroll
+                for (int kt = 0; kt < D / 8; ++kt) {
+                    uint32_t ah[4], al[4];
+                    split_tf32(Sd[kt][0], ah[0], al[0]);
+                    split_tf32(Sd[kt][2], ah[1], al[1]);
+                    split_tf32(Sd[kt][1], ah[2], al[2]);
+                    split_tf32(Sd[kt][3], ah[3], al[3]);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+#pragma unroll
+                        for (int n = 0; n < 2; ++n) {
+                            const float2 bv = *reinterpret_cast<const float2*>(
+                                sm + (x ? OFF_QG : OFF_KG) + (8 * n + fg) * XS + 8 * kt + 2 * fc);
+                            uint32_t bh[2], bl[2];
+                            split_tf32(bv.x, bh[0], bl[0]);
+                            split_tf32(bv.y, bh[1], bl[1]);
+                            mma3(Y[x][n], ah, al, bh, bl);
+                        }
                 }
-                float ks[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+                // to the warp's scratch as [kind][token][column]
 #pragma unroll
-                for (int r = 0; r < 16; ++r)
+                for (int x = 0; x < 2; ++x)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        ks[c] = fmaf(S[r][c], ak[r], ks[c]);
-                        qs[c] = fmaf(S[r][c], aq[r], qs[c]);
-                    }
-                float* red = sm + OFF_RED;
-                *reinterpret_cast<float4*>(red + warp * RED + c0) = make_float4(ks[0], ks[1], ks[2], ks[3]);
-                *reinterpret_cast<float4*>(red + (NW + warp) * RED + c0) = make_float4(qs[0], qs[1], qs[2], qs[3]);
-                __syncthreads();
-                {
-                    const int colx = threadIdx.x >> 1, part = threadIdx.x & 1;
-                    float sk = 0.f, sq = 0.f;
+                    for (int n = 0; n < 2; ++n)
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        sk += red[(part * 4 + m) * RED + colx];
-                        sq += red[(NW + part * 4 + m) * RED + colx];
-                    }
-                    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-                    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-                    if (part == 0) {
-                        const float uu = sm[OFF_B + j] * (sm[OFF_V + j * D + colx] - sk);
-                        sm[OFF_U + colx] = uu;
-                        if (tb0 + j >= seg_a)  // the piece's prefix tokens are not stored
-                            o[((size_t)(tb0 + j) * p.h_v + h) * D + colx] = from_f32<TOut>(p.scale * fmaf(sm[OFF_KQ + j], uu, sq));
-                    }
+                        for (int e = 0; e < 4; ++e)
+                            ws[x * C * 16 + (8 * n + 2 * fc + (e & 1)) * 16 + fg + 8 * (e >> 1)] = Y[x][n][e];
+            }
+            __syncthreads();  // A and P of the chunk; the warp's scratch
+            // per column (lanes 0-15 of the warp): E = (I + A)^{-1} (V - K_G S0) by forward
+            // substitution, Y + P E in place of Y, and beta E for the update
+            if (lane < 16) {
+                const int col = 16 * warp + lane;
+                float e[C];
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    float r = sm[OFF_V + t * D + col] - ws[t * 16 + lane];
+#pragma unroll
+                    for (int s_ = 0; s_ < t; ++s_) r = fmaf(-sm[OFF_AM + t * C + s_], e[s_], r);
+                    e[t] = r;
                 }
-                __syncthreads();
-                const float4 u4 = *reinterpret_cast<const float4*>(sm + OFF_U + c0);
-                const float u[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-                for (int r = 0; r < 16; r += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(sm + OFF_A + j * D + r0 + r);
-                    const float4 k4 = *reinterpret_cast<const float4*>(sm + OFF_K + j * D + r0 + r);
-                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+                for (int t = 0; t < C; ++t) {
+                    float y = ws[C * 16 + t * 16 + lane];
 #pragma unroll
-                    for (int rr = 0; rr < 4; ++rr)
+                    for (int s_ = 0; s_ <= t; ++s_) y = fmaf(sm[OFF_PM + t * C + s_], e[s_], y);
+                    ws[C * 16 + t * 16 + lane] = y;
+                    ws[2 * C * 16 + t * 16 + lane] = sm[OFF_BT + t] * e[t];
+                }
+            }
+            __syncwarp();
+            {  // the outputs of the warp's columns, two tokens at a time over the 32 lanes
+                const int cl = lane & 15;
+                TOut* ob = o + ((size_t)tb0 * p.h_v + h) * D + 16 * warp + cl;
+                const size_t ostride = (size_t)p.h_v * D;
+#pragma unroll 1
+                for (int t = lane >> 4; t < nt; t += 2)
+                    if (tb0 + t >= seg_a)  // the piece's prefix tokens are not stored
+                        ob[(size_t)t * ostride] = from_f32<TOut>(p.scale * ws[C * 16 + t * 16 + cl]);
+            }
+            // S^T <- S^T diag(exp(G_L)) + U^T K_T on the warp MMA (U = diag(beta) E)
+            {
+                uint32_t uh[2][4], ul[2][4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) S[r + rr][c] = fmaf(av[rr], S[r + rr][c], kv[rr] * u[c]);
+                for (int kt = 0; kt < 2; ++kt) {
+                    const float* u = ws + 2 * C * 16 + (8 * kt + 2 * fc) * 16 + fg;
+                    split_tf32(u[0], uh[kt][0], ul[kt][0]);
+                    split_tf32(u[8], uh[kt][1], ul[kt][1]);
+                    split_tf32(u[16], uh[kt][2], ul[kt][2]);
+                    split_tf32(u[24], uh[kt][3], ul[kt][3]);
+                }
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    const float2 gl = *reinterpret_cast<const float2*>(sm + OFF_GL + 8 * j + 2 * fc);
+                    Sd[j][0] *= gl.x; Sd[j][1] *= gl.y; Sd[j][2] *= gl.x; Sd[j][3] *= gl.y;
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        const float2 bv = *reinterpret_cast<const float2*>(sm + OFF_KTT + (8 * j + fg) * KS + 8 * kt + 2 * fc);
+                        uint32_t bh[2], bl[2];
+                        split_tf32(bv.x, bh[0], bl[0]);
+                        split_tf32(bv.y, bh[1], bl[1]);
+                        mma3(Sd[j], uh[kt], ul[kt], bh, bl);
+                    }
                 }
             }
         }
-        if (p.hT && t1 == s1) bwd::store_state(S, p.hT + st_off, r0, c0);  // the piece ends its sequence
+        if (p.hT && t1 == s1) {  // the piece ends its sequence
+            float* dst = p.hT + st_off;
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[(size_t)(8 * j + 2 * fc + (e & 1)) * D + 16 * warp + fg + 8 * (e >> 1)] = Sd[j][e];
+        }
         pc0 = pc1;
     }
 }
