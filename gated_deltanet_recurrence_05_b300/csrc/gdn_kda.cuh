@@ -150,16 +150,18 @@ constexpr int OFF_K = 0;               // k   [C][D]
 constexpr int OFF_Q = OFF_K + C * D;   // q   [C][D]
 constexpr int OFF_V = OFF_Q + C * D;   // v   [C][D]
 constexpr int OFF_G2 = OFF_V + C * D;  // g as loaded, then G / ln 2 [C][D] (running sums, base 2)
-constexpr int OFF_KG = OFF_G2 + C * D; // K_G [C][XS]
-constexpr int OFF_QG = OFF_KG + C * XS;
-constexpr int OFF_KI = OFF_QG + C * XS;  // K_I = rows k_t o exp(-G_t) [C][XS]
+constexpr int OFF_KG = OFF_G2 + C * D; // K_G [C][XS], tf32 high parts
+constexpr int OFF_KGL = OFF_KG + C * XS; // and the low parts (K_G = high + low)
+constexpr int OFF_QG = OFF_KGL + C * XS; // Q_G likewise
+constexpr int OFF_QGL = OFF_QG + C * XS;
+constexpr int OFF_KI = OFF_QGL + C * XS; // K_I = rows k_t o exp(-G_t) [C][XS]
 constexpr int OFF_KTT = OFF_KI + C * XS; // K_T^T [D][KS]
 constexpr int OFF_GL = OFF_KTT + D * KS; // exp(G_L) [D]
 constexpr int OFF_AM = OFF_GL + D;       // A [C][C]
 constexpr int OFF_PM = OFF_AM + C * C;   // P [C][C]
 constexpr int OFF_BT = OFF_PM + C * C;   // beta [C]
-constexpr int OFF_WS = OFF_BT + C;       // per warp: S0^T K_G, S0^T Q_G [2][C][16], then beta E [C][16]
-constexpr int WS_FLOATS = 3 * C * 16;
+constexpr int OFF_WS = OFF_BT + C;       // per warp: S0^T K_G (then beta E), S0^T Q_G [2][C][16]
+constexpr int WS_FLOATS = 2 * C * 16;
 constexpr int SMEM_FLOATS = OFF_WS + NW * WS_FLOATS;
 constexpr size_t SMEM_BYTES = (size_t)SMEM_FLOATS * sizeof(float);
 static_assert(OFF_KG % 4 == 0 && OFF_KTT % 4 == 0 && OFF_WS % 4 == 0 && XS % 4 == 0 && KS % 2 == 0,
@@ -304,8 +306,13 @@ __device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long l
         const float gm = sm[OFF_G2 + j * D + i];
         const float e = ex2f(gm), kj = sm[OFF_K + j * D + i];
         wide |= fabsf(gm) > G2_MAX;
-        sm[OFF_KG + j * XS + i] = kj * e;
-        sm[OFF_QG + j * XS + i] = sm[OFF_Q + j * D + i] * e;
+        uint32_t hi, lo;
+        split_tf32(kj * e, hi, lo);
+        sm[OFF_KG + j * XS + i] = __uint_as_float(hi);
+        sm[OFF_KGL + j * XS + i] = __uint_as_float(lo);
+        split_tf32(sm[OFF_Q + j * D + i] * e, hi, lo);
+        sm[OFF_QG + j * XS + i] = __uint_as_float(hi);
+        sm[OFF_QGL + j * XS + i] = __uint_as_float(lo);
         sm[OFF_KTT + i * KS + j] = kj * ex2f(acc - gm);
         sm[OFF_KI + j * XS + i] = kj * ex2f(-gm);
     }
@@ -321,19 +328,18 @@ __device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long l
 __device__ __forceinline__ void kda_chunk_ap_mma(float* sm, int warp, int lane) {
     const int fg = lane >> 2, fc = lane & 3;
     const int isP = warp >> 1, nb = warp & 1;
-    const float* X = sm + (isP ? OFF_QG : OFF_KG);
+    const float* Xh = sm + (isP ? OFF_QG : OFF_KG);
+    const float* Xl = sm + (isP ? OFF_QGL : OFF_KGL);
     const float* Ki = sm + OFF_KI + (8 * nb + fg) * XS;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int kt = 0; kt < D / 8; ++kt) {
-        const float2 x0 = *reinterpret_cast<const float2*>(X + fg * XS + 8 * kt + 2 * fc);
-        const float2 x1 = *reinterpret_cast<const float2*>(X + (fg + 8) * XS + 8 * kt + 2 * fc);
+        const int o0 = fg * XS + 8 * kt + 2 * fc, o1 = o0 + 8 * XS;
+        const uint2 h0 = *reinterpret_cast<const uint2*>(Xh + o0), h1 = *reinterpret_cast<const uint2*>(Xh + o1);
+        const uint2 l0 = *reinterpret_cast<const uint2*>(Xl + o0), l1 = *reinterpret_cast<const uint2*>(Xl + o1);
         const float2 bv = *reinterpret_cast<const float2*>(Ki + 8 * kt + 2 * fc);
-        uint32_t ah[4], al[4], bh[2], bl[2];
-        split_tf32(x0.x, ah[0], al[0]);
-        split_tf32(x1.x, ah[1], al[1]);
-        split_tf32(x0.y, ah[2], al[2]);
-        split_tf32(x1.y, ah[3], al[3]);
+        const uint32_t ah[4] = {h0.x, h1.x, h0.y, h1.y}, al[4] = {l0.x, l1.x, l0.y, l1.y};
+        uint32_t bh[2], bl[2];
         split_tf32(bv.x, bh[0], bl[0]);
         split_tf32(bv.y, bh[1], bl[1]);
         mma3(d, ah, al, bh, bl);
@@ -347,13 +353,12 @@ __device__ __forceinline__ void kda_chunk_ap_mma(float* sm, int warp, int lane) 
     M[(fg + 8) * C + s0 + 1] = b1 * d[3];
 }
 
-// A (thread tid < 120) or P (the other 136) entry of the staged chunk: one
-// dot product over the 128 channels, the channels rotated by lane so that the
-// lanes' 16-byte reads spread over all banks. The decay factor
-// exp(G_t - G_s) = exp(G_t) exp(-G_s) is folded into the rows K_G, Q_G and
-// K_I, unless some running sum of the chunk is beyond +-G2_MAX (base 2), where
-// exp(-G) could overflow: then each factor is taken per element.
-__device__ __forceinline__ void kda_chunk_ap(float* sm, int lane, bool wide) {
+// A (thread tid < 120) or P (the other 136) entry of the staged chunk with
+// the decay factors taken per element (a chunk whose running decays pass
+// +-G2_MAX, where exp(-G) could overflow): one dot product over the 128
+// channels, the channels rotated by lane so that the lanes' 16-byte reads
+// spread over all banks.
+__device__ __forceinline__ void kda_chunk_ap_wide(float* sm, int lane) {
     const bool isA = threadIdx.x < (C * (C - 1)) / 2;
     int jj = isA ? (int)threadIdx.x : (int)threadIdx.x - (C * (C - 1)) / 2, t = 0;
     while (jj >= (isA ? t : t + 1)) {  // entries of row t: s < t (A) or s <= t (P)
@@ -361,36 +366,20 @@ __device__ __forceinline__ void kda_chunk_ap(float* sm, int lane, bool wide) {
         ++t;
     }
     const int s = jj;
+    const float* X = sm + (isA ? OFF_K : OFF_Q) + t * D;
+    const float* Ks = sm + OFF_K + s * D;
+    const float* Gt = sm + OFF_G2 + t * D;
+    const float* Gs = sm + OFF_G2 + s * D;
     float acc = 0.f;
-    if (!wide) {
-        const float* X = sm + (isA ? OFF_KG : OFF_QG) + t * XS;
-        const float* Ks = sm + OFF_KI + s * XS;
-        float acc2 = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < D / 4; ++m) {
-            const int i = ((m + lane) & (D / 4 - 1)) * 4;
-            const float4 x = *reinterpret_cast<const float4*>(X + i), kk = *reinterpret_cast<const float4*>(Ks + i);
-            acc = fmaf(x.x, kk.x, acc);
-            acc2 = fmaf(x.y, kk.y, acc2);
-            acc = fmaf(x.z, kk.z, acc);
-            acc2 = fmaf(x.w, kk.w, acc2);
-        }
-        acc += acc2;
-    } else {
-        const float* X = sm + (isA ? OFF_K : OFF_Q) + t * D;
-        const float* Ks = sm + OFF_K + s * D;
-        const float* Gt = sm + OFF_G2 + t * D;
-        const float* Gs = sm + OFF_G2 + s * D;
 #pragma unroll 4
-        for (int m = 0; m < D / 4; ++m) {
-            const int i = ((m + lane) & (D / 4 - 1)) * 4;
-            const float4 x = *reinterpret_cast<const float4*>(X + i), kk = *reinterpret_cast<const float4*>(Ks + i);
-            const float4 gt = *reinterpret_cast<const float4*>(Gt + i), gs = *reinterpret_cast<const float4*>(Gs + i);
-            acc = fmaf(x.x * kk.x, ex2f(gt.x - gs.x), acc);
-            acc = fmaf(x.y * kk.y, ex2f(gt.y - gs.y), acc);
-            acc = fmaf(x.z * kk.z, ex2f(gt.z - gs.z), acc);
-            acc = fmaf(x.w * kk.w, ex2f(gt.w - gs.w), acc);
-        }
+    for (int m = 0; m < D / 4; ++m) {
+        const int i = ((m + lane) & (D / 4 - 1)) * 4;
+        const float4 x = *reinterpret_cast<const float4*>(X + i), kk = *reinterpret_cast<const float4*>(Ks + i);
+        const float4 gt = *reinterpret_cast<const float4*>(Gt + i), gs = *reinterpret_cast<const float4*>(Gs + i);
+        acc = fmaf(x.x * kk.x, ex2f(gt.x - gs.x), acc);
+        acc = fmaf(x.y * kk.y, ex2f(gt.y - gs.y), acc);
+        acc = fmaf(x.z * kk.z, ex2f(gt.z - gs.z), acc);
+        acc = fmaf(x.w * kk.w, ex2f(gt.w - gs.w), acc);
     }
     sm[(isA ? OFF_AM : OFF_PM) + t * C + s] = sm[OFF_BT + s] * acc;
 }
@@ -481,7 +470,7 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
             const int nt = (int)min((long long)C, t1 - tb0);
             __syncthreads();  // the previous chunk's tiles are free
             const bool wide = kda_stage_chunk<TIn>(sm, p, tb0, nt, h, hk);  // ends with a block barrier
-            if (wide) kda_chunk_ap(sm, lane, true);
+            if (wide) kda_chunk_ap_wide(sm, lane);
             else if (warp < 4) kda_chunk_ap_mma(sm, warp, lane);
             // S0^T K_G^T and S0^T Q_G^T (16 columns x 16 tokens each) on the warp MMA
             {
@@ -503,11 +492,10 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
                     for (int x = 0; x < 2; ++x)
 #pragma unroll
                         for (int n = 0; n < 2; ++n) {
-                            const float2 bv = *reinterpret_cast<const float2*>(
-                                sm + (x ? OFF_QG : OFF_KG) + (8 * n + fg) * XS + 8 * kt + 2 * fc);
-                            uint32_t bh[2], bl[2];
-                            split_tf32(bv.x, bh[0], bl[0]);
-                            split_tf32(bv.y, bh[1], bl[1]);
+                            const int ob = (8 * n + fg) * XS + 8 * kt + 2 * fc;
+                            const uint2 h = *reinterpret_cast<const uint2*>(sm + (x ? OFF_QG : OFF_KG) + ob);
+                            const uint2 l = *reinterpret_cast<const uint2*>(sm + (x ? OFF_QGL : OFF_KGL) + ob);
+                            const uint32_t bh[2] = {h.x, h.y}, bl[2] = {l.x, l.y};
                             mma3(Y[x][n], ah, al, bh, bl);
                         }
                 }
@@ -539,7 +527,7 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
 #pragma unroll
                     for (int s_ = 0; s_ <= t; ++s_) y = fmaf(sm[OFF_PM + t * C + s_], e[s_], y);
                     ws[C * 16 + t * 16 + lane] = y;
-                    ws[2 * C * 16 + t * 16 + lane] = sm[OFF_BT + t] * e[t];
+                    ws[t * 16 + lane] = sm[OFF_BT + t] * e[t];  // beta E over S0^T K_G (read above)
                 }
             }
             __syncwarp();
@@ -557,7 +545,7 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
                 uint32_t uh[2][4], ul[2][4];
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
-                    const float* u = ws + 2 * C * 16 + (8 * kt + 2 * fc) * 16 + fg;
+                    const float* u = ws + (8 * kt + 2 * fc) * 16 + fg;
                     split_tf32(u[0], uh[kt][0], ul[kt][0]);
                     split_tf32(u[8], uh[kt][1], ul[kt][1]);
                     split_tf32(u[16], uh[kt][2], ul[kt][2]);
