@@ -510,7 +510,7 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
             }
             __syncthreads();  // A and P of the chunk; the warp's scratch
             // per column (lanes 0-15 of the warp): E = (I + A)^{-1} (V - K_G S0) by forward
-            // substitution, Y + P E in place of Y, and beta E for the update
+            // substitution, over S0^T K_G in the warp's scratch
             if (lane < 16) {
                 const int col = 16 * warp + lane;
                 float e[C];
@@ -518,38 +518,53 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
                 for (int t = 0; t < C; ++t) {
                     float r = sm[OFF_V + t * D + col] - ws[t * 16 + lane];
 #pragma unroll
-                    for (int s_ = 0; s_ < t; ++s_) r = fmaf(-sm[OFF_AM + t * C + s_], e[s_], r);
+                    for (int s4 = 0; s4 < t; s4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(sm + OFF_AM + t * C + s4);
+                        r = fmaf(-a4.x, e[s4], r);
+                        if (s4 + 1 < t) r = fmaf(-a4.y, e[s4 + 1], r);
+                        if (s4 + 2 < t) r = fmaf(-a4.z, e[s4 + 2], r);
+                        if (s4 + 3 < t) r = fmaf(-a4.w, e[s4 + 3], r);
+                    }
                     e[t] = r;
                 }
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    float y = ws[C * 16 + t * 16 + lane];
-#pragma unroll
-                    for (int s_ = 0; s_ <= t; ++s_) y = fmaf(sm[OFF_PM + t * C + s_], e[s_], y);
-                    ws[C * 16 + t * 16 + lane] = y;
-                    ws[t * 16 + lane] = sm[OFF_BT + t] * e[t];  // beta E over S0^T K_G (read above)
-                }
+                for (int t = 0; t < C; ++t) ws[t * 16 + lane] = e[t];
             }
             __syncwarp();
-            {  // the outputs of the warp's columns, two tokens at a time over the 32 lanes
-                const int cl = lane & 15;
+            {  // O = scale (Q_G S0 + P E) for column cl and the tokens t = hp, hp + 2, ..., stored
+                const int cl = lane & 15, hp = lane >> 4;
+                float e[C];
+#pragma unroll
+                for (int u = 0; u < C; ++u) e[u] = ws[u * 16 + cl];
                 TOut* ob = o + ((size_t)tb0 * p.h_v + h) * D + 16 * warp + cl;
                 const size_t ostride = (size_t)p.h_v * D;
-#pragma unroll 1
-                for (int t = lane >> 4; t < nt; t += 2)
-                    if (tb0 + t >= seg_a)  // the piece's prefix tokens are not stored
-                        ob[(size_t)t * ostride] = from_f32<TOut>(p.scale * ws[C * 16 + t * 16 + cl]);
+#pragma unroll
+                for (int m = 0; m < C / 2; ++m) {
+                    const int t = 2 * m + hp;
+                    float y = ws[C * 16 + t * 16 + cl];
+#pragma unroll
+                    for (int s4 = 0; s4 <= 2 * m + 1; s4 += 4) {  // s <= t; P vanishes above the diagonal
+                        const float4 p4 = *reinterpret_cast<const float4*>(sm + OFF_PM + t * C + s4);
+                        if (s4 <= t) y = fmaf(p4.x, e[s4], y);
+                        if (s4 + 1 <= t) y = fmaf(p4.y, e[s4 + 1], y);
+                        if (s4 + 2 <= t) y = fmaf(p4.z, e[s4 + 2], y);
+                        if (s4 + 3 <= t) y = fmaf(p4.w, e[s4 + 3], y);
+                    }
+                    if (t < nt && tb0 + t >= seg_a)  // the piece's prefix tokens are not stored
+                        ob[(size_t)t * ostride] = from_f32<TOut>(p.scale * y);
+                }
             }
             // S^T <- S^T diag(exp(G_L)) + U^T K_T on the warp MMA (U = diag(beta) E)
             {
                 uint32_t uh[2][4], ul[2][4];
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
-                    const float* u = ws + (8 * kt + 2 * fc) * 16 + fg;
-                    split_tf32(u[0], uh[kt][0], ul[kt][0]);
-                    split_tf32(u[8], uh[kt][1], ul[kt][1]);
-                    split_tf32(u[16], uh[kt][2], ul[kt][2]);
-                    split_tf32(u[24], uh[kt][3], ul[kt][3]);
+                    const float* u = ws + (8 * kt + 2 * fc) * 16 + fg;  // E
+                    const float b0 = sm[OFF_BT + 8 * kt + 2 * fc], b1 = sm[OFF_BT + 8 * kt + 2 * fc + 1];
+                    split_tf32(b0 * u[0], uh[kt][0], ul[kt][0]);
+                    split_tf32(b0 * u[8], uh[kt][1], ul[kt][1]);
+                    split_tf32(b1 * u[16], uh[kt][2], ul[kt][2]);
+                    split_tf32(b1 * u[24], uh[kt][3], ul[kt][3]);
                 }
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
