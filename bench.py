@@ -848,8 +848,9 @@ def run_kda(args, dev, peaks, world, w, dd):
         prefill()
     reps = max(3, min(args.steps, 10))
     us_pf = timed(lambda i: prefill(), reps, "prefill")
-    flops = 6.0 * d_k * d_v * T * h_v   # S^T (a o k), S^T (a o q), the decayed rank-1 update
+    flops = 6.0 * d_k * d_v * T * h_v   # the two reads of the state and its update, per token and head
     tfs = flops / (us_pf / 1e6) / 1e12
+    tf32_peak = peaks["bf16_tflops"] * (1.1 / 2.25)
 
     wl = gdn_inputs.WORKLOADS["decode"]
     steps = 100
@@ -874,9 +875,13 @@ def run_kda(args, dev, peaks, world, w, dd):
                                     f"fp32 log-decays [T, {h_v}, {d_k}], bf16 o, fp32 final states",
                         "us_per_launch": us_pf, "tokens_per_s": T * world / (us_pf / 1e6), "gpu_launches": reps,
                         "timing": timings["prefill"], "cold_first_call": cold,
-                        "roofline": {"bound": "alu", "achieved": round(tfs, 2), "peak": round(SIMT_FP32_TFLOPS, 1),
-                                     "unit": "TFLOP/s", "frac": round(tfs / SIMT_FP32_TFLOPS, 4),
-                                     "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 FLOP x 2032 MHz",
+                        "roofline": {"bound": "tensor", "achieved": round(tfs, 2), "peak": round(tf32_peak, 1),
+                                     "unit": "TFLOP/s", "frac": round(tfs / tf32_peak, 4),
+                                     "peak_source": "derived: the measured bf16 peak x the nominal tf32/bf16 ratio "
+                                                    "(1.1 / 2.25); the state products run as three tf32 warp-MMA "
+                                                    "passes each (fp32 accuracy)",
+                                     "fp32_simt_peak": round(SIMT_FP32_TFLOPS, 1),
+                                     "frac_of_fp32_simt": round(tfs / SIMT_FP32_TFLOPS, 4),
                                      "algorithmic_flops_per_launch": flops}},
             "decode": {"workload": f"KDA decode: {wl.num_seqs} x {wl.h_v} states of 128x128 fp32, per-channel "
                                    f"decays, {steps} in-place steps",

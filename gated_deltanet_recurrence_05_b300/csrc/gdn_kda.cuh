@@ -8,9 +8,10 @@
 //   S~  = diag(a_t) S_{t-1},  a_t = exp(g_t) in R^{d_k}
 //   e_t = v_t - S~^T k_t,     S_t = S~ + b_t k_t e_t^T,     o_t = scale S_t^T q_t
 //
-// Since S~^T x = S^T (a o x), the reads use a o k and a o q, and
-// S_t^T q = S^T (a o q) + (k . q) u with u = b e: one pass over S for both
-// reads, one for the update. d_k = d_v = 128.
+// The decode step uses S~^T x = S^T (a o x): the reads use a o k and a o q,
+// and S_t^T q = S^T (a o q) + (k . q) u with u = b e, one pass over S for both
+// reads and one for the update. The prefill takes chunks of 16 tokens in the
+// WY form (below). d_k = d_v = 128.
 #pragma once
 
 #include "gdn_common.cuh"

@@ -400,9 +400,14 @@ size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
  * gdn_decode_step except g, which is per key channel:
  *   prefill: g [T_total, H_v, d_k] fp32     decode: g [N, H_v, d_k] fp32
  * Both need d_k = d_v = 128 (GDN_ERR_UNSUPPORTED otherwise) and 16-byte
- * aligned g. The prefill runs token by token on the fp32 CUDA cores (one CTA
- * per sequence and value head, state in registers); the decode step reads
- * and writes each state once, like gdn_decode_step.
+ * aligned g. The prefill runs chunks of 16 tokens in the WY form of the rule
+ * (one CTA of 256 threads per sequence and value head, or per balanced share
+ * or sequence segment as for gdn_chunk_fwd; state in registers), the state
+ * products and the intra-chunk scores on the warp MMA with tf32 operands split
+ * into high and low parts (fp32 accuracy: every result within the fp32
+ * bound of the token-by-token rule); a chunk whose running decays pass 2^-100
+ * takes its decay factors per element. The decode step reads and writes each
+ * state once, like gdn_decode_step.
  */
 gdn_status gdn_kda_chunk_fwd(const void* q, const void* k, const void* v,
                              const float* g, const float* beta,
