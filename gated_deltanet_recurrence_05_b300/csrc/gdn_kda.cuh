@@ -142,8 +142,9 @@ kda_decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, con
 // column on lanes 0-15 of each warp; the chunk's tiles (k, q, v, the decays,
 // A and P) are shared through shared memory.
 constexpr int C = 16;                  // tokens per chunk
-constexpr int XS = D + 8;              // row stride of K_G, Q_G, K_I ([token][channel]): conflict-free fragments
-constexpr int KS = C + 8;              // row stride of K_T^T ([channel][token])
+constexpr int XS = D + 8;              // row stride (floats) of K_I ([token][channel]): conflict-free fragments
+constexpr int RW = (D + 8) / 2;        // row stride (32-bit words of two fp16) of K_G, Q_G ([token][channel])
+constexpr int RT = (C + 8) / 2;        // row stride (words) of K_T^T ([channel][token])
 // |running log2-decay| up to which exp(-G) and exp(G) stay normal fp32
 // numbers (2^100 and 2^-100) and their product keeps full precision
 constexpr float G2_MAX = 100.f;
@@ -151,21 +152,29 @@ constexpr int OFF_K = 0;               // k   [C][D]
 constexpr int OFF_Q = OFF_K + C * D;   // q   [C][D]
 constexpr int OFF_V = OFF_Q + C * D;   // v   [C][D]
 constexpr int OFF_G2 = OFF_V + C * D;  // g as loaded, then G / ln 2 [C][D] (running sums, base 2)
-constexpr int OFF_KG = OFF_G2 + C * D; // K_G [C][XS], tf32 high parts
-constexpr int OFF_KGL = OFF_KG + C * XS; // and the low parts (K_G = high + low)
-constexpr int OFF_QG = OFF_KGL + C * XS; // Q_G likewise
-constexpr int OFF_QGL = OFF_QG + C * XS;
-constexpr int OFF_KI = OFF_QGL + C * XS; // K_I = rows k_t o exp(-G_t) [C][XS]
-constexpr int OFF_KTT = OFF_KI + C * XS; // K_T^T [D][KS]
-constexpr int OFF_GL = OFF_KTT + D * KS; // exp(G_L) [D]
-constexpr int OFF_AM = OFF_GL + D;       // A [C][C]
+// K_G, Q_G, K_T^T are kept as fp16 pairs (high, low) scaled by the chunk's
+// powers of two 2^ek, 2^eq (x = high + low to about 22 bits)
+constexpr int OFF_KG = OFF_G2 + C * D;   // K_G 2^ek, high parts [C][RW words]
+constexpr int OFF_KGL = OFF_KG + C * RW; // and the low parts
+constexpr int OFF_QG = OFF_KGL + C * RW; // Q_G 2^eq likewise
+constexpr int OFF_QGL = OFF_QG + C * RW;
+constexpr int OFF_KTT = OFF_QGL + C * RW;  // K_T^T 2^ek, high parts [D][RT words]
+constexpr int OFF_KTL = OFF_KTT + D * RT;  // and the low parts
+constexpr int OFF_KI = OFF_KTL + D * RT;   // K_I = rows k_t o exp(-G_t) [C][XS] fp32
+// K_G and Q_G in fp32 for A and P, where they meet K_I: exp(G_t) can be far
+// below the fp16 range while exp(G_t - G_s) is not
+constexpr int OFF_KG32 = OFF_KI + C * XS;
+constexpr int OFF_QG32 = OFF_KG32 + C * XS;
+constexpr int OFF_GL = OFF_QG32 + C * XS;  // exp(G_L) [D]
+constexpr int OFF_MX = OFF_GL + D;         // per warp max |k|, max |q|, max growth of the chunk [3][NW]
+constexpr int OFF_AM = OFF_MX + 3 * NW;  // A [C][C]
 constexpr int OFF_PM = OFF_AM + C * C;   // P [C][C]
 constexpr int OFF_BT = OFF_PM + C * C;   // beta [C]
 constexpr int OFF_WS = OFF_BT + C;       // per warp: S0^T K_G (then beta E), S0^T Q_G [2][C][16]
 constexpr int WS_FLOATS = 2 * C * 16;
 constexpr int SMEM_FLOATS = OFF_WS + NW * WS_FLOATS;
 constexpr size_t SMEM_BYTES = (size_t)SMEM_FLOATS * sizeof(float);
-static_assert(OFF_KG % 4 == 0 && OFF_KTT % 4 == 0 && OFF_WS % 4 == 0 && XS % 4 == 0 && KS % 2 == 0,
+static_assert(OFF_KG % 4 == 0 && OFF_KI % 4 == 0 && OFF_WS % 4 == 0 && XS % 4 == 0,
               "vector alignment");
 static_assert(2 * SMEM_BYTES + 2048 <= 232448, "two CTAs per SM");
 
@@ -181,6 +190,38 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
     const float r = x - __uint_as_float(hi);
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+// 2^e, exact for e in [-126, 127] (clamped outside, which only extreme
+// magnitudes of the state or the inputs reach)
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + max(-126, min(127, e))) << 23); }
+// the power of two 2^e that brings max |x| = m into [2^14, 2^15) (1 for m = 0)
+__device__ __forceinline__ int scale_exp(float m) {
+    return m > 0.f ? max(-60, min(60, 14 - ilogbf(m))) : 0;
+}
+// fp16 pairs (x0, x1) = high + low 2^-11, packed as two half2 words: the low
+// part is stored scaled by 2^11 so that it stays a normal fp16 number (the
+// tensor cores flush fp16 subnormals) wherever x itself is
+constexpr float LO_UP = 2048.f, LO_DOWN = 1.f / 2048.f;
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x0, x1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn((x0 - hf.x) * LO_UP, (x1 - hf.y) * LO_UP);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+// D += A B on the warp MMA, m16n8k16, fp16 operands, fp32 accumulators
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// the cross terms high x low of split operands (both scaled by 2^11)
+__device__ __forceinline__ void mma_cross(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                          const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    mma_f16(d, al, bh[0], bh[1]);
+    mma_f16(d, ah, bl[0], bl[1]);
 }
 // D += A B on the warp MMA, m16n8k8, tf32 operands, fp32 accumulators
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -261,11 +302,13 @@ __device__ __forceinline__ long long segment_prefix_start(const Args& p, long lo
 // chunk's decayed rows (thread (half hf, channel i): the tokens of its half).
 // Returns whether some running sum is beyond +-G2_MAX (a block-wide OR).
 template <typename TIn>
-__device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long long tb0, int n, int h, int hk) {
+__device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long long tb0, int n, int h, int hk,
+                                                int& ek, int& eq) {
     constexpr float LOG2E = 1.4426950408889634f;
     const TIn* q = static_cast<const TIn*>(p.q);
     const TIn* k = static_cast<const TIn*>(p.k);
     const TIn* v = static_cast<const TIn*>(p.v);
+    float mk = 0.f, mq = 0.f;  // max |k|, |q| of the thread's part of the chunk
     for (int idx = threadIdx.x; idx < C * (D / 4); idx += NT) {
         const int j = idx >> 5, c = (idx & 31) * 4;
         float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), qq = kk, vv = kk, gg = kk;
@@ -278,28 +321,73 @@ __device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long l
             vv = load4(v + v_off);
             gg = *reinterpret_cast<const float4*>(p.g + v_off);
         }
+        mk = fmaxf(mk, fmaxf(fmaxf(fabsf(kk.x), fabsf(kk.y)), fmaxf(fabsf(kk.z), fabsf(kk.w))));
+        mq = fmaxf(mq, fmaxf(fmaxf(fabsf(qq.x), fabsf(qq.y)), fmaxf(fabsf(qq.z), fabsf(qq.w))));
         *reinterpret_cast<float4*>(sm + OFF_K + j * D + c) = kk;
         *reinterpret_cast<float4*>(sm + OFF_Q + j * D + c) = qq;
         *reinterpret_cast<float4*>(sm + OFF_V + j * D + c) = vv;
         *reinterpret_cast<float4*>(sm + OFF_G2 + j * D + c) = gg;
     }
     if (threadIdx.x < C) sm[OFF_BT + threadIdx.x] = threadIdx.x < n ? p.beta[(size_t)(tb0 + threadIdx.x) * p.h_v + h] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+        mq = fmaxf(mq, __shfl_xor_sync(0xffffffffu, mq, off));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        sm[OFF_MX + (threadIdx.x >> 5)] = mk;
+        sm[OFF_MX + NW + (threadIdx.x >> 5)] = mq;
+    }
     __syncthreads();
+    // the chunk's scales 2^ek, 2^eq: max |K_G|, |K_T| <= max |k|, max |Q_G| <= max |q|
+    {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            a = fmaxf(a, sm[OFF_MX + w]);
+            b = fmaxf(b, sm[OFF_MX + NW + w]);
+        }
+        ek = scale_exp(a);
+        eq = scale_exp(b);
+    }
     const int hf = threadIdx.x >> 7, i = threadIdx.x & (D - 1);
     if (hf == 0) {  // running sums of g, in place, one thread per channel
         float gv[C];
 #pragma unroll
         for (int j = 0; j < C; ++j) gv[j] = sm[OFF_G2 + j * D + i];
-        float acc = 0.f;
+        float acc = 0.f, gmax = 0.f, gmin = 0.f;
 #pragma unroll
         for (int j = 0; j < C; ++j) {
             acc = fmaf(gv[j], LOG2E, acc);
             sm[OFF_G2 + j * D + i] = acc;
+            gmax = fmaxf(gmax, acc);
+            gmin = fminf(gmin, acc);
         }
         sm[OFF_GL + i] = ex2f(acc);
+        // largest log2 factor by which a row of K_G, Q_G or K_T exceeds |k| or |q|
+        // (0 for decays; positive only where some g > 0)
+        float up = fmaxf(gmax, acc - gmin);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) up = fmaxf(up, __shfl_xor_sync(0xffffffffu, up, off));
+        if ((threadIdx.x & 31) == 0) sm[OFF_MX + 2 * NW + (threadIdx.x >> 5)] = up;
     }
     __syncthreads();
+    {
+        float up = 0.f;
+#pragma unroll
+        for (int w = 0; w < D / 32; ++w) up = fmaxf(up, sm[OFF_MX + 2 * NW + w]);
+        const int sh = (int)ceilf(fminf(up, 60.f));
+        ek = max(-100, ek - sh);
+        eq = max(-100, eq - sh);
+    }
     const float acc = sm[OFF_G2 + (C - 1) * D + i];
+    const float sk = pow2i(ek), sq = pow2i(eq);
+    __half* kgh = reinterpret_cast<__half*>(sm + OFF_KG);
+    __half* kgl = reinterpret_cast<__half*>(sm + OFF_KGL);
+    __half* qgh = reinterpret_cast<__half*>(sm + OFF_QG);
+    __half* qgl = reinterpret_cast<__half*>(sm + OFF_QGL);
+    __half* kth = reinterpret_cast<__half*>(sm + OFF_KTT);
+    __half* ktl = reinterpret_cast<__half*>(sm + OFF_KTL);
     bool wide = false;  // a running sum outside [-G2_MAX, G2_MAX]: exp(-G) could overflow
 #pragma unroll
     for (int jj = 0; jj < C / 2; ++jj) {
@@ -307,14 +395,17 @@ __device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long l
         const float gm = sm[OFF_G2 + j * D + i];
         const float e = ex2f(gm), kj = sm[OFF_K + j * D + i];
         wide |= fabsf(gm) > G2_MAX;
-        uint32_t hi, lo;
-        split_tf32(kj * e, hi, lo);
-        sm[OFF_KG + j * XS + i] = __uint_as_float(hi);
-        sm[OFF_KGL + j * XS + i] = __uint_as_float(lo);
-        split_tf32(sm[OFF_Q + j * D + i] * e, hi, lo);
-        sm[OFF_QG + j * XS + i] = __uint_as_float(hi);
-        sm[OFF_QGL + j * XS + i] = __uint_as_float(lo);
-        sm[OFF_KTT + i * KS + j] = kj * ex2f(acc - gm);
+        const float kg1 = kj * e, qg1 = sm[OFF_Q + j * D + i] * e;
+        sm[OFF_KG32 + j * XS + i] = kg1;
+        sm[OFF_QG32 + j * XS + i] = qg1;
+        const float kg = kg1 * sk, qg = qg1 * sq, kt = kj * ex2f(acc - gm) * sk;
+        const __half kgh_ = __float2half_rn(kg), qgh_ = __float2half_rn(qg), kth_ = __float2half_rn(kt);
+        kgh[j * 2 * RW + i] = kgh_;
+        kgl[j * 2 * RW + i] = __float2half_rn((kg - __half2float(kgh_)) * LO_UP);
+        qgh[j * 2 * RW + i] = qgh_;
+        qgl[j * 2 * RW + i] = __float2half_rn((qg - __half2float(qgh_)) * LO_UP);
+        kth[i * 2 * RT + j] = kth_;
+        ktl[i * 2 * RT + j] = __float2half_rn((kt - __half2float(kth_)) * LO_UP);
         sm[OFF_KI + j * XS + i] = kj * ex2f(-gm);
     }
     return __syncthreads_or(wide) != 0;
@@ -329,18 +420,20 @@ __device__ __forceinline__ bool kda_stage_chunk(float* sm, const Args& p, long l
 __device__ __forceinline__ void kda_chunk_ap_mma(float* sm, int warp, int lane) {
     const int fg = lane >> 2, fc = lane & 3;
     const int isP = warp >> 1, nb = warp & 1;
-    const float* Xh = sm + (isP ? OFF_QG : OFF_KG);
-    const float* Xl = sm + (isP ? OFF_QGL : OFF_KGL);
+    const float* X = sm + (isP ? OFF_QG32 : OFF_KG32);
     const float* Ki = sm + OFF_KI + (8 * nb + fg) * XS;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
     for (int kt = 0; kt < D / 8; ++kt) {
-        const int o0 = fg * XS + 8 * kt + 2 * fc, o1 = o0 + 8 * XS;
-        const uint2 h0 = *reinterpret_cast<const uint2*>(Xh + o0), h1 = *reinterpret_cast<const uint2*>(Xh + o1);
-        const uint2 l0 = *reinterpret_cast<const uint2*>(Xl + o0), l1 = *reinterpret_cast<const uint2*>(Xl + o1);
+        // channels 8kt + 2c, 8kt + 2c + 1 of tokens g and g + 8 (the k order 2c, 2c + 1)
+        const float2 x0 = *reinterpret_cast<const float2*>(X + fg * XS + 8 * kt + 2 * fc);
+        const float2 x1 = *reinterpret_cast<const float2*>(X + (fg + 8) * XS + 8 * kt + 2 * fc);
         const float2 bv = *reinterpret_cast<const float2*>(Ki + 8 * kt + 2 * fc);
-        const uint32_t ah[4] = {h0.x, h1.x, h0.y, h1.y}, al[4] = {l0.x, l1.x, l0.y, l1.y};
-        uint32_t bh[2], bl[2];
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        split_tf32(x0.x, ah[0], al[0]);
+        split_tf32(x1.x, ah[1], al[1]);
+        split_tf32(x0.y, ah[2], al[2]);
+        split_tf32(x1.y, ah[3], al[3]);
         split_tf32(bv.x, bh[0], bl[0]);
         split_tf32(bv.y, bh[1], bl[1]);
         mma3(d, ah, al, bh, bl);
@@ -470,44 +563,62 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
         for (long long tb0 = t0; tb0 < t1; tb0 += C) {
             const int nt = (int)min((long long)C, t1 - tb0);
             __syncthreads();  // the previous chunk's tiles are free
-            const bool wide = kda_stage_chunk<TIn>(sm, p, tb0, nt, h, hk);  // ends with a block barrier
+            int ek, eq;
+            const bool wide = kda_stage_chunk<TIn>(sm, p, tb0, nt, h, hk, ek, eq);  // ends with a block barrier
             if (wide) kda_chunk_ap_wide(sm, lane);
             else if (warp < 4) kda_chunk_ap_mma(sm, warp, lane);
             // S0^T K_G^T and S0^T Q_G^T (16 columns x 16 tokens each) on the warp MMA
             {
-                float Y[2][2][4];
+                float Y[2][2][4], Yx[2][2][4];  // high x high; the cross terms (scaled by 2^11)
 #pragma unroll
                 for (int x = 0; x < 2; ++x)
 #pragma unroll
                     for (int n = 0; n < 2; ++n)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) Y[x][n][e] = 0.f;
+                        for (int e = 0; e < 4; ++e) Y[x][n][e] = Yx[x][n][e] = 0.f;
+                // the warp's slice of S scaled by 2^es into the fp16 range
+                float m = 0.f;
 #pragma unroll
-                for (int kt = 0; kt < D / 8; ++kt) {
+                for (int j = 0; j < D / 8; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(Sd[j][e]));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                const int es = scale_exp(m);
+                const float ss = pow2i(es);
+                const uint32_t* Kh = reinterpret_cast<const uint32_t*>(sm + OFF_KG);
+                const uint32_t* Kl = reinterpret_cast<const uint32_t*>(sm + OFF_KGL);
+                const uint32_t* Qh = reinterpret_cast<const uint32_t*>(sm + OFF_QG);
+                const uint32_t* Ql = reinterpret_cast<const uint32_t*>(sm + OFF_QGL);
+#pragma unroll
+                for (int kt = 0; kt < D / 16; ++kt) {  // rows 16 kt .. 16 kt + 15 = fragments 2kt, 2kt + 1
                     uint32_t ah[4], al[4];
-                    split_tf32(Sd[kt][0], ah[0], al[0]);
-                    split_tf32(Sd[kt][2], ah[1], al[1]);
-                    split_tf32(Sd[kt][1], ah[2], al[2]);
-                    split_tf32(Sd[kt][3], ah[3], al[3]);
+                    split_f16x2(Sd[2 * kt][0] * ss, Sd[2 * kt][1] * ss, ah[0], al[0]);
+                    split_f16x2(Sd[2 * kt][2] * ss, Sd[2 * kt][3] * ss, ah[1], al[1]);
+                    split_f16x2(Sd[2 * kt + 1][0] * ss, Sd[2 * kt + 1][1] * ss, ah[2], al[2]);
+                    split_f16x2(Sd[2 * kt + 1][2] * ss, Sd[2 * kt + 1][3] * ss, ah[3], al[3]);
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
 #pragma unroll
                         for (int n = 0; n < 2; ++n) {
-                            const int ob = (8 * n + fg) * XS + 8 * kt + 2 * fc;
-                            const uint2 h = *reinterpret_cast<const uint2*>(sm + (x ? OFF_QG : OFF_KG) + ob);
-                            const uint2 l = *reinterpret_cast<const uint2*>(sm + (x ? OFF_QGL : OFF_KGL) + ob);
-                            const uint32_t bh[2] = {h.x, h.y}, bl[2] = {l.x, l.y};
-                            mma3(Y[x][n], ah, al, bh, bl);
+                            const int ob = (8 * n + fg) * RW + 8 * kt + fc;
+                            const uint32_t* H = x ? Qh : Kh;
+                            const uint32_t* L = x ? Ql : Kl;
+                            const uint32_t bh[2] = {H[ob], H[ob + 4]}, bl[2] = {L[ob], L[ob + 4]};
+                            mma_cross(Yx[x][n], ah, al, bh, bl);
+                            mma_f16(Y[x][n], ah, bh[0], bh[1]);
                         }
                 }
-                // to the warp's scratch as [kind][token][column]
+                // to the warp's scratch as [kind][token][column], scales undone
+                const float rk = pow2i(-es - ek), rq = pow2i(-es - eq);
 #pragma unroll
                 for (int x = 0; x < 2; ++x)
 #pragma unroll
                     for (int n = 0; n < 2; ++n)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            ws[x * C * 16 + (8 * n + 2 * fc + (e & 1)) * 16 + fg + 8 * (e >> 1)] = Y[x][n][e];
+                            ws[x * C * 16 + (8 * n + 2 * fc + (e & 1)) * 16 + fg + 8 * (e >> 1)] =
+                                fmaf(Yx[x][n][e], LO_DOWN, Y[x][n][e]) * (x ? rq : rk);
             }
             __syncthreads();  // A and P of the chunk; the warp's scratch
             // per column (lanes 0-15 of the warp): E = (I + A)^{-1} (V - K_G S0) by forward
@@ -555,30 +666,44 @@ __global__ void __launch_bounds__(NT, 2) kda_prefill_kernel(const Args p) {
                         ob[(size_t)t * ostride] = from_f32<TOut>(p.scale * y);
                 }
             }
-            // S^T <- S^T diag(exp(G_L)) + U^T K_T on the warp MMA (U = diag(beta) E)
+            // S^T <- S^T diag(exp(G_L)) + U^T K_T on the warp MMA (U = diag(beta) E); U scaled by
+            // 2^eu into the fp16 range, K_T by 2^ek, and S^T by both for the accumulation
             {
-                uint32_t uh[2][4], ul[2][4];
-#pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
-                    const float* u = ws + (8 * kt + 2 * fc) * 16 + fg;  // E
-                    const float b0 = sm[OFF_BT + 8 * kt + 2 * fc], b1 = sm[OFF_BT + 8 * kt + 2 * fc + 1];
-                    split_tf32(b0 * u[0], uh[kt][0], ul[kt][0]);
-                    split_tf32(b0 * u[8], uh[kt][1], ul[kt][1]);
-                    split_tf32(b1 * u[16], uh[kt][2], ul[kt][2]);
-                    split_tf32(b1 * u[24], uh[kt][3], ul[kt][3]);
+                float uv[8];
+                {
+                    const float* u = ws + 2 * fc * 16 + fg;  // E[token][column]
+                    const float b0 = sm[OFF_BT + 2 * fc], b1 = sm[OFF_BT + 2 * fc + 1];
+                    const float b8 = sm[OFF_BT + 2 * fc + 8], b9 = sm[OFF_BT + 2 * fc + 9];
+                    uv[0] = b0 * u[0];   uv[1] = b1 * u[16];       // column g, tokens 2c, 2c + 1
+                    uv[2] = b0 * u[8];   uv[3] = b1 * u[24];       // column g + 8
+                    uv[4] = b8 * u[128]; uv[5] = b9 * u[144];      // column g, tokens 2c + 8, 2c + 9
+                    uv[6] = b8 * u[136]; uv[7] = b9 * u[152];      // column g + 8
                 }
+                float m = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(uv[e]));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                const int eu = scale_exp(m);
+                const float su = pow2i(eu), sup = pow2i(eu + ek), rup = pow2i(-eu - ek);
+                uint32_t uh[4], ul[4];
+                split_f16x2(uv[0] * su, uv[1] * su, uh[0], ul[0]);
+                split_f16x2(uv[2] * su, uv[3] * su, uh[1], ul[1]);
+                split_f16x2(uv[4] * su, uv[5] * su, uh[2], ul[2]);
+                split_f16x2(uv[6] * su, uv[7] * su, uh[3], ul[3]);
+                const uint32_t* Th = reinterpret_cast<const uint32_t*>(sm + OFF_KTT);
+                const uint32_t* Tl = reinterpret_cast<const uint32_t*>(sm + OFF_KTL);
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
                     const float2 gl = *reinterpret_cast<const float2*>(sm + OFF_GL + 8 * j + 2 * fc);
-                    Sd[j][0] *= gl.x; Sd[j][1] *= gl.y; Sd[j][2] *= gl.x; Sd[j][3] *= gl.y;
-#pragma unroll
-                    for (int kt = 0; kt < 2; ++kt) {
-                        const float2 bv = *reinterpret_cast<const float2*>(sm + OFF_KTT + (8 * j + fg) * KS + 8 * kt + 2 * fc);
-                        uint32_t bh[2], bl[2];
-                        split_tf32(bv.x, bh[0], bl[0]);
-                        split_tf32(bv.y, bh[1], bl[1]);
-                        mma3(Sd[j], uh[kt], ul[kt], bh, bl);
-                    }
+                    const float g0 = gl.x * sup * LO_UP, g1 = gl.y * sup * LO_UP;
+                    Sd[j][0] *= g0; Sd[j][1] *= g1; Sd[j][2] *= g0; Sd[j][3] *= g1;
+                    const int ob = (8 * j + fg) * RT + fc;  // tokens 2c, 2c + 1 (and + 8) of row 8j + g
+                    const uint32_t bh[2] = {Th[ob], Th[ob + 4]}, bl[2] = {Tl[ob], Tl[ob + 4]};
+                    mma_cross(Sd[j], uh, ul, bh, bl);  // at the scale 2^11 of the low parts
+                    Sd[j][0] *= LO_DOWN; Sd[j][1] *= LO_DOWN; Sd[j][2] *= LO_DOWN; Sd[j][3] *= LO_DOWN;
+                    mma_f16(Sd[j], uh, bh[0], bh[1]);
+                    Sd[j][0] *= rup; Sd[j][1] *= rup; Sd[j][2] *= rup; Sd[j][3] *= rup;
                 }
             }
         }

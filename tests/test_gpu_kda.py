@@ -2,8 +2,10 @@
 gdn_kda_decode_step) against the fp64 KDA oracle (oracle.kda_recurrent).
 
 Both kernels keep an fp32 state (bf16 inputs widened exactly); the prefill's
-products run on the warp MMA as three tf32 passes over split operands, which
-carry about 22 significant bits, so outputs and final states are held to
+products run on the warp MMA as three passes over operands split into high
+and low parts (fp16 with power-of-two scales for the state products, tf32 for
+the intra-chunk scores), about 22 significant bits, so outputs and final
+states are held to
 max|err| <= 1e-4 x RMS(ref) (the fp32 bound of the forward tests); a bf16 output is compared with the oracle
 rounded to bf16 plus one bf16 ulp. Inputs: the seeded recipe of gdn_inputs
 with per-channel log-decays g = -softplus(N(0,1) + shift) per key channel.
@@ -101,6 +103,23 @@ def test_prefill_strong_and_zero_decay_chunks():
     g[90:160] = weak[90:160]           # sequence 0: strong, weak, strong
     g[200:350] = 0.0                   # sequence 1: no decay
     g[350:, :, 64:] = weak[350:, :, 64:]  # sequence 2: channels 0-63 strong, 64-127 weak
+    o, S = _kda_gpu(d, g)
+    o_ref, S_ref = oracle.kda_recurrent(d["q"], d["k"], d["v"], g, d["beta"], h0=d["h0"], cu_seqlens=_cu(d))
+    assert_parity(o, o_ref, TAU_F32, "o")
+    assert_parity(S, S_ref, TAU_F32, "final state")
+
+
+@pytest.mark.parametrize("g_shift", [2.0, 4.0])
+def test_prefill_moderate_decays_within_a_chunk(g_shift):
+    """Decays of the prefill benchmark's distribution (g_shift 2: the running
+    decay of a 16-token chunk falls to about 2^-50) and stronger ones near the
+    chunk's per-element threshold (g_shift 4): A and P pair rows scaled by
+    exp(G_t) and exp(-G_s), which must keep their full range even where
+    exp(G_t) alone is far below the fp16 range; every output and final state
+    against the oracle at the fp32 bound."""
+    d = gdn_inputs.make_prefill(h_qk=1, h_v=2, d_k=128, d_v=128, dtype="bf16", lengths=[100, 37],
+                                h0_std=0.02, seed=48)
+    g = gdn_inputs.make_channel_decay((137, 2, 128), g_shift=g_shift, seed=48)
     o, S = _kda_gpu(d, g)
     o_ref, S_ref = oracle.kda_recurrent(d["q"], d["k"], d["v"], g, d["beta"], h0=d["h0"], cu_seqlens=_cu(d))
     assert_parity(o, o_ref, TAU_F32, "o")
