@@ -875,11 +875,12 @@ def run_kda(args, dev, peaks, world, w, dd):
                                     f"fp32 log-decays [T, {h_v}, {d_k}], bf16 o, fp32 final states",
                         "us_per_launch": us_pf, "tokens_per_s": T * world / (us_pf / 1e6), "gpu_launches": reps,
                         "timing": timings["prefill"], "cold_first_call": cold,
-                        "roofline": {"bound": "tensor", "achieved": round(tfs, 2), "peak": round(tf32_peak, 1),
-                                     "unit": "TFLOP/s", "frac": round(tfs / tf32_peak, 4),
-                                     "peak_source": "derived: the measured bf16 peak x the nominal tf32/bf16 ratio "
-                                                    "(1.1 / 2.25); the state products run as three tf32 warp-MMA "
-                                                    "passes each (fp32 accuracy)",
+                        "roofline": {"bound": "tensor", "achieved": round(tfs, 2), "peak": peaks["bf16_tflops"],
+                                     "unit": "TFLOP/s", "frac": round(tfs / peaks["bf16_tflops"], 4),
+                                     "peak_source": "measured (bf16, the fp16 rate): the state products run on "
+                                                    "fp16 warp MMA as three passes over split operands (fp32 "
+                                                    "accuracy), the intra-chunk scores on tf32",
+                                     "tf32_peak": round(tf32_peak, 1),
                                      "fp32_simt_peak": round(SIMT_FP32_TFLOPS, 1),
                                      "frac_of_fp32_simt": round(tfs / SIMT_FP32_TFLOPS, 4),
                                      "algorithmic_flops_per_launch": flops}},

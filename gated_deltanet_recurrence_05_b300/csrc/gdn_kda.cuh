@@ -130,17 +130,23 @@ kda_decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, con
 //
 // One CTA of 256 threads per piece; warp w owns state columns 16w..16w+15
 // and keeps S^T (16 columns x 128 rows) in fp32 registers as the accumulator
-// fragments of the warp MMA (m16n8k8, tf32): lane (g, c) = (lane / 4,
-// lane % 4) holds rows 8j + 2c, 8j + 2c + 1 of columns 16w + g, 16w + g + 8,
-// j = 0..15. The three state products of a chunk, S0^T K_G^T, S0^T Q_G^T and
-// U^T K_T (U = diag(beta) E), run on the tensor cores with fp32 accuracy:
-// each fp32 operand x is split into tf32 parts x = hi + lo and the product
-// taken as hi hi + hi lo + lo hi (fp32 accumulation). The contraction index
-// of each 8-wide step is taken in the order (2c, 2c + 1 for c = 0..3) on both
-// operands, which makes the state's accumulator fragments its A fragments
-// without any data movement. The triangular solve and the outputs run per
-// column on lanes 0-15 of each warp; the chunk's tiles (k, q, v, the decays,
-// A and P) are shared through shared memory.
+// fragments of the warp MMA: lane (g, c) = (lane / 4, lane % 4) holds rows
+// 8j + 2c, 8j + 2c + 1 of columns 16w + g, 16w + g + 8, j = 0..15, which are
+// also the A fragments of an m16n8k16 product over rows 16i .. 16i + 15
+// (fragments 2i, 2i + 1), so the state feeds its own reads with no data
+// movement. The three state products of a chunk, S0^T K_G^T, S0^T Q_G^T and
+// U^T K_T (U = diag(beta) E), run in fp32 accuracy on fp16 m16n8k16: each
+// operand is scaled by a power of two into [2^14, 2^15) at its maximum (per
+// warp for S and U, per chunk for K_G, Q_G, K_T), split into fp16 parts
+// x = hi + lo 2^-11 (the low part stored scaled so that it stays a normal
+// number: the tensor cores flush fp16 subnormals), and the product taken as
+// hi hi + (hi lo + lo hi) 2^-11 with fp32 accumulation; the scales are undone
+// exactly. A and P (K_G K_I^T, Q_G K_I^T) pair exp(G_t) with exp(-G_s), whose
+// ranges only fp32 holds: they run on m16n8k8 tf32 with each operand split
+// into tf32 parts (the contraction order 2c, 2c + 1 within each 8-wide step).
+// The triangular solve runs per column on lanes 0-15 of each warp, the
+// outputs on all lanes; the chunk's tiles (k, q, v, the decays, A and P) are
+// shared through shared memory.
 constexpr int C = 16;                  // tokens per chunk
 constexpr int XS = D + 8;              // row stride (floats) of K_I ([token][channel]): conflict-free fragments
 constexpr int RW = (D + 8) / 2;        // row stride (32-bit words of two fp16) of K_G, Q_G ([token][channel])

@@ -403,8 +403,9 @@ size_t gdn_chunk_bwd_workspace_size(int32_t num_seqs, int64_t total_tokens,
  * aligned g. The prefill runs chunks of 16 tokens in the WY form of the rule
  * (one CTA of 256 threads per sequence and value head, or per balanced share
  * or sequence segment as for gdn_chunk_fwd; state in registers), the state
- * products and the intra-chunk scores on the warp MMA with tf32 operands split
- * into high and low parts (fp32 accuracy: every result within the fp32
+ * products and the intra-chunk scores on the warp MMA with operands split
+ * into high and low parts (fp16 under power-of-two scales for the state
+ * products, tf32 for the scores; fp32 accuracy: every result within the fp32
  * bound of the token-by-token rule); a chunk whose running decays pass 2^-100
  * takes its decay factors per element. The decode step reads and writes each
  * state once, like gdn_decode_step.
