@@ -139,7 +139,8 @@ kda_decode_d128_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, con
 // operand is scaled by a power of two into [2^14, 2^15) at its maximum (per
 // warp for S and U, per chunk for K_G, Q_G, K_T), split into fp16 parts
 // x = hi + lo 2^-11 (the low part stored scaled so that it stays a normal
-// number: the tensor cores flush fp16 subnormals), and the product taken as
+// fp16 number: unscaled, many low parts are subnormal, and the products then
+// missed fp32 accuracy on the tensor cores), and the product taken as
 // hi hi + (hi lo + lo hi) 2^-11 with fp32 accumulation; the scales are undone
 // exactly. A and P (K_G K_I^T, Q_G K_I^T) pair exp(G_t) with exp(-G_s), whose
 // ranges only fp32 holds: they run on m16n8k8 tf32 with each operand split
@@ -205,8 +206,9 @@ __device__ __forceinline__ int scale_exp(float m) {
     return m > 0.f ? max(-60, min(60, 14 - ilogbf(m))) : 0;
 }
 // fp16 pairs (x0, x1) = high + low 2^-11, packed as two half2 words: the low
-// part is stored scaled by 2^11 so that it stays a normal fp16 number (the
-// tensor cores flush fp16 subnormals) wherever x itself is
+// part is stored scaled by 2^11 so that it stays a normal fp16 number
+// wherever x itself is (unscaled, it falls into the subnormal range, where
+// the tensor-core products lost precision)
 constexpr float LO_UP = 2048.f, LO_DOWN = 1.f / 2048.f;
 __device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
     const __half2 h = __floats2half2_rn(x0, x1);
